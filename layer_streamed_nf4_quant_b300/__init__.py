@@ -1,0 +1,238 @@
+"""Layer-streamed NF4-LoRA for B300 (sm_103a): Python binding of liblsn.so.
+
+The functions here marshal torch tensors (device memory, streams) and numpy arrays into the
+C ABI declared in ``include/lsn.h``; every step of the computation runs in the library's
+CUDA kernels and host code.  Importing this package fails if the library is not built.
+
+bf16 tensors are ``torch.bfloat16``; packed NF4 matrices and layer images are ``torch.uint8``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from ._lib import (LSN_ECORRUPT, LSN_EINVAL, LSN_ENOMEM, LSN_ESTATE, LSN_ETIMEOUT, LSN_OK,  # noqa: F401
+                   LsnError, check, lib, lsn_pool_stats, lsn_stack_desc, nf4_view)
+
+PROJ = ("q", "k", "v", "gate", "up", "o", "down")   # canonical projection order
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------------------ NF4
+
+def codebook() -> np.ndarray:
+    out = (C.c_float * 16)()
+    check(lib.lsn_nf4_codebook(out))
+    return np.frombuffer(out, dtype=np.float32).copy()
+
+
+def nf4_packed_bytes(n_out: int, k_in: int) -> int:
+    return int(lib.nf4_packed_bytes(n_out, k_in))
+
+
+def nf4_pack(W: np.ndarray, n_threads: int = 0, out: np.ndarray | None = None) -> np.ndarray:
+    """Host quantiser: fp32 [n_out x k_in] -> packed bytes (numpy uint8)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    n, k = W.shape
+    nbytes = nf4_packed_bytes(n, k)
+    if nbytes == 0:
+        raise LsnError(LSN_EINVAL, "k_in must be a positive multiple of 64")
+    if out is None:
+        out = np.empty(nbytes, dtype=np.uint8)
+    check(lib.nf4_pack(W.ctypes.data_as(C.c_void_p), n, k, out.ctypes.data_as(C.c_void_p), out.nbytes, n_threads))
+    return out
+
+
+def view(packed, n_out: int, k_in: int) -> nf4_view:
+    return nf4_view(C.c_void_p(packed.data_ptr()), n_out, k_in)
+
+
+def nf4_dequant(packed, n_out: int, k_in: int, out=None, stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty((n_out, k_in), dtype=torch.bfloat16, device=packed.device)
+    v = view(packed, n_out, k_in)
+    check(lib.nf4_dequant(C.byref(v), _p(out), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------------ LoRA linear
+
+def lora_workspace(M: int, n_out: int, k_in: int, r: int, device="cuda"):
+    torch = _torch()
+    n = int(lib.lora_nf4_workspace_bytes(M, n_out, k_in, r))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def lora_nf4_fwd(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, T=None, ws=None, stream=None):
+    """Y = bf16(X W^T + s T B^T [+ residual]), T = bf16(X A^T).  Returns (Y, T)."""
+    torch = _torch()
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, n_out), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.bfloat16, device=X.device)
+    if ws is None:
+        ws = lora_workspace(M, n_out, k_in, r, X.device)
+    v = view(packed, n_out, k_in)
+    check(lib.lora_nf4_fwd(C.byref(v), _p(X), M, _p(A), _p(B), r, float(scale), _p(residual), _p(Y), _p(T),
+                           _p(ws), ws.numel(), _stream(stream)))
+    return Y, T
+
+
+def lora_nf4_bwd(packed, n_out, k_in, X, T, dY, A, B, r, scale, dX=None, accumulate_dX=False, dA=None,
+                 dB=None, ws=None, want_dX=True, stream=None):
+    """dX (+)= dY W + dT A, dA = dT^T X, dB = s dY^T T with dT = bf16(s dY B).  Returns (dX, dA, dB)."""
+    torch = _torch()
+    M = X.shape[0]
+    dev = X.device
+    if want_dX and dX is None:
+        dX = torch.empty((M, k_in), dtype=torch.float32, device=dev)
+    if dA is None:
+        dA = torch.empty((r, k_in), dtype=torch.float32, device=dev)
+    if dB is None:
+        dB = torch.empty((n_out, r), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = lora_workspace(M, n_out, k_in, r, dev)
+    v = view(packed, n_out, k_in)
+    check(lib.lora_nf4_bwd(C.byref(v), _p(X), _p(T), _p(dY), M, _p(A), _p(B), r, float(scale),
+                           _p(dX if want_dX else None), 1 if accumulate_dX else 0, _p(dA), _p(dB), _p(ws),
+                           ws.numel(), _stream(stream)))
+    return dX, dA, dB
+
+
+def device_check(stream=None) -> int:
+    """Synchronises and returns the device error status (raises LsnError on an error)."""
+    detail = C.c_uint32(0)
+    check(lib.lsn_check(_stream(stream), C.byref(detail)))
+    return detail.value
+
+
+# ------------------------------------------------------------------------ stream pool
+
+class StreamPool:
+    """Two-slot VRAM pool over a pinned host store (owner of the C handle)."""
+
+    def __init__(self, store, offsets, layer_bytes: int, slot0, slot1, copy_stream, first_slot: int = 0,
+                 reuse_resident: bool = False):
+        self._keep = (store, slot0, slot1, copy_stream)
+        n = len(offsets)
+        offs = (C.c_size_t * n)(*[int(o) for o in offsets])
+        h = C.c_void_p()
+        check(lib.stream_pool_create(C.c_void_p(store.data_ptr()), store.numel() * store.element_size(), offs,
+                                     layer_bytes, n, _p(slot0), _p(slot1), C.c_void_p(copy_stream.cuda_stream),
+                                     first_slot, 1 if reuse_resident else 0, C.byref(h)))
+        self.handle = h
+
+    def prefetch(self, layer: int):
+        check(lib.stream_pool_prefetch(self.handle, layer))
+
+    def wait(self, layer: int, stream=None, timeout_ms: int = 0) -> int:
+        p = C.c_void_p()
+        check(lib.stream_pool_wait(self.handle, layer, _stream(stream), C.byref(p), timeout_ms))
+        return p.value
+
+    def release(self, layer: int, stream=None):
+        check(lib.stream_pool_release(self.handle, layer, _stream(stream)))
+
+    def set_copy_delay_us(self, usec: int):
+        check(lib.stream_pool_set_copy_delay_us(self.handle, usec))
+
+    def stats(self) -> dict:
+        s = lsn_pool_stats()
+        check(lib.stream_pool_stats(self.handle, C.byref(s)))
+        return {"bytes_copied": s.bytes_copied, "copies": s.copies, "skipped": s.skipped,
+                "copy_ms": s.copy_ms, "wait_ms": s.wait_ms}
+
+    def reset_stats(self):
+        check(lib.stream_pool_reset_stats(self.handle))
+
+    def close(self):
+        if self.handle:
+            check(lib.stream_pool_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------------ layer stack
+
+class StackDesc:
+    """Shapes of the synthetic decoder-layer stack and the layouts the library derives."""
+
+    def __init__(self, n_layers=32, d_model=4096, d_kv=1024, d_ff=14336, rank=64, lora_alpha=16.0,
+                 rms_eps=1e-5, kv_loss_coef=1e-3):
+        self.c = lsn_stack_desc(n_layers, d_model, d_kv, d_ff, rank, lora_alpha, rms_eps, kv_loss_coef)
+        self.n_layers, self.d_model, self.d_kv, self.d_ff, self.rank = n_layers, d_model, d_kv, d_ff, rank
+        self.scale = lora_alpha / rank
+        self.image_bytes = int(lib.lsn_layer_image_bytes(C.byref(self.c)))
+        if self.image_bytes == 0:
+            raise LsnError(LSN_EINVAL, "bad stack descriptor")
+        offs = (C.c_size_t * 7)()
+        check(lib.lsn_layer_image_offsets(C.byref(self.c), offs))
+        self.image_offsets = list(offs)
+        self.lora_elems = int(lib.lsn_lora_elems(C.byref(self.c)))
+        lo = (C.c_size_t * 14)()
+        check(lib.lsn_lora_offsets(C.byref(self.c), lo))
+        self.lora_offsets = list(lo)
+
+    def shape(self, p: str):
+        D, dkv, F = self.d_model, self.d_kv, self.d_ff
+        return {"q": (D, D), "k": (dkv, D), "v": (dkv, D), "gate": (F, D), "up": (F, D), "o": (D, D),
+                "down": (D, F)}[p]
+
+    def workspace_bytes(self, M: int) -> int:
+        return int(lib.lsn_stack_workspace_bytes(C.byref(self.c), M))
+
+    def pack_layer(self, layer: int, W: dict, dst: np.ndarray | None = None, n_threads: int = 0) -> np.ndarray:
+        """Packs one layer image (header + seven NF4 matrices) from fp32 numpy weights."""
+        mats = [np.ascontiguousarray(W[p], dtype=np.float32) for p in PROJ]
+        for p, m in zip(PROJ, mats):
+            if m.shape != self.shape(p):
+                raise LsnError(LSN_EINVAL, f"W[{p}] has shape {m.shape}, expected {self.shape(p)}")
+        ptrs = (C.c_void_p * 7)(*[m.ctypes.data for m in mats])
+        if dst is None:
+            dst = np.empty(self.image_bytes, dtype=np.uint8)
+        check(lib.lsn_layer_image_pack(C.byref(self.c), layer, ptrs, dst.ctypes.data_as(C.c_void_p), dst.nbytes,
+                                       n_threads))
+        return dst
+
+    def lora_views(self, blob):
+        """Views of A_p [r x K_p] and B_p [N_p x r] inside one layer's LoRA (or grad) blob."""
+        A, B = {}, {}
+        r = self.rank
+        for i, p in enumerate(PROJ):
+            n, k = self.shape(p)
+            A[p] = blob[self.lora_offsets[i]: self.lora_offsets[i] + r * k].view(r, k)
+            B[p] = blob[self.lora_offsets[7 + i]: self.lora_offsets[7 + i] + n * r].view(n, r)
+        return A, B
+
+
+def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
+                     resident_store=None, x_out=None, dx0=None, stream=None):
+    """One forward + loss + backward pass over the stack (streamed through `pool`, or resident)."""
+    L = desc.n_layers
+    lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
+    gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
+    check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
+                               _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws), ws.numel(),
+                               _stream(stream)))

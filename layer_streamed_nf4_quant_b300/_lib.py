@@ -1,0 +1,97 @@
+"""ctypes declarations of liblsn.so (argument marshalling only; every computation runs in
+the library).  Loading fails loudly if the library has not been built."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblsn.so")
+
+LSN_OK = 0
+LSN_EINVAL = -1
+LSN_ENOMEM = -2
+LSN_ECUDA = -3
+LSN_ETIMEOUT = -4
+LSN_ESTATE = -5
+LSN_ECORRUPT = -6
+STATUS_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ETIMEOUT", -5: "ESTATE",
+                -6: "ECORRUPT"}
+
+
+class LsnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class nf4_view(C.Structure):
+    _fields_ = [("base", C.c_void_p), ("n_out", C.c_int64), ("k_in", C.c_int64)]
+
+
+class lsn_pool_stats(C.Structure):
+    _fields_ = [("bytes_copied", C.c_uint64), ("copies", C.c_uint64), ("skipped", C.c_uint64),
+                ("copy_ms", C.c_double), ("wait_ms", C.c_double)]
+
+
+class lsn_stack_desc(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("d_kv", C.c_int32),
+                ("d_ff", C.c_int32), ("rank", C.c_int32), ("lora_alpha", C.c_float),
+                ("rms_eps", C.c_float), ("kv_loss_coef", C.c_float)]
+
+
+P = C.c_void_p
+I = C.c_int
+I64 = C.c_int64
+SZ = C.c_size_t
+F = C.c_float
+
+# name -> (restype, argtypes); mirrors include/lsn.h
+SIGNATURES = {
+    "lsn_last_error": (C.c_char_p, []),
+    "lsn_abi_version": (I, []),
+    "lsn_check": (I, [P, C.POINTER(C.c_uint32)]),
+    "lsn_nf4_codebook": (I, [C.POINTER(F)]),
+    "nf4_packed_bytes": (SZ, [I64, I64]),
+    "nf4_pack": (I, [P, I64, I64, P, SZ, I]),
+    "nf4_dequant": (I, [C.POINTER(nf4_view), P, P]),
+    "lora_nf4_workspace_bytes": (SZ, [I64, I64, I64, I]),
+    "lora_nf4_fwd": (I, [C.POINTER(nf4_view), P, I64, P, P, I, F, P, P, P, P, SZ, P]),
+    "lora_nf4_bwd": (I, [C.POINTER(nf4_view), P, P, P, I64, P, P, I, F, P, I, P, P, P, SZ, P]),
+    "stream_pool_create": (I, [P, SZ, C.POINTER(SZ), SZ, I, P, P, P, I, I, C.POINTER(P)]),
+    "stream_pool_prefetch": (I, [P, I]),
+    "stream_pool_wait": (I, [P, I, P, C.POINTER(P), I]),
+    "stream_pool_release": (I, [P, I, P]),
+    "stream_pool_stats": (I, [P, C.POINTER(lsn_pool_stats)]),
+    "stream_pool_reset_stats": (I, [P]),
+    "stream_pool_set_copy_delay_us": (I, [P, I]),
+    "stream_pool_destroy": (I, [P]),
+    "lsn_layer_image_bytes": (SZ, [C.POINTER(lsn_stack_desc)]),
+    "lsn_layer_image_offsets": (I, [C.POINTER(lsn_stack_desc), C.POINTER(SZ)]),
+    "lsn_layer_image_pack": (I, [C.POINTER(lsn_stack_desc), I, C.POINTER(P), P, SZ, I]),
+    "lsn_lora_elems": (SZ, [C.POINTER(lsn_stack_desc)]),
+    "lsn_lora_offsets": (I, [C.POINTER(lsn_stack_desc), C.POINTER(SZ)]),
+    "lsn_stack_workspace_bytes": (SZ, [C.POINTER(lsn_stack_desc), I64]),
+    "layer_stack_step": (I, [P, P, C.POINTER(lsn_stack_desc), P, I64, C.POINTER(P), C.POINTER(P), P, P, P,
+                             P, SZ, P]),
+}
+
+
+def load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m layer_streamed_nf4_quant_b300.build`")
+    lib = C.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = load()
+
+
+def check(rc: int) -> None:
+    if rc != LSN_OK:
+        raise LsnError(rc, lib.lsn_last_error().decode(errors="replace"))

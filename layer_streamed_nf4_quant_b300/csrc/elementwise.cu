@@ -1,0 +1,361 @@
+// Memory-bound kernels of the synthetic decoder layer: RMSNorm forward/backward, SiLU-mul,
+// the loss and its seed gradients, and the assembly of the fused QKVGU output gradient.
+// Every reduction runs in a fixed order (fixed grid, fixed shuffle tree), so results are
+// bit-reproducible.
+//
+// Layer definition (the workload description of the Llama-3.1-8B-shaped layer): unit-weight
+// RMSNorm with eps, q/k/v/gate/up projections, a = silu(gate) * up, x' = x + o(q) + down(a);
+// loss = 0.5 mean(x_L^2) + sum_l c (mean(k_l^2) + mean(v_l^2)).
+#include <cuda_bf16.h>
+
+#include "lsn_internal.h"
+#include "stack_kernels.h"
+
+namespace lsn {
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Fixed-order warp sum to lane 0, broadcast back to every lane.
+__device__ __forceinline__ float warp_sum_bcast(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+    return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// Fixed-order block sum (blockDim.x == 256) of one value per thread; result valid in thread 0.
+__device__ __forceinline__ float block_sum256(float v, float* sh) {
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int s = 128; s > 0; s >>= 1) {
+        if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+        __syncthreads();
+    }
+    return sh[0];
+}
+
+// ------------------------------------------------------------------------ layer tag
+
+__global__ void tag_check_kernel(const LayerHeader* hdr, uint32_t expect_layer, uint32_t* err) {
+    if (threadIdx.x == 0 && (hdr->magic != kImageMagic || hdr->layer != expect_layer))
+        atomicCAS(err, 0u, (kDevErrTag << 24) | (expect_layer & 0xFFFFFFu));
+}
+
+// ------------------------------------------------------------------------- RMSNorm
+
+__global__ void rmsnorm_fwd_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ h,
+                                   float* __restrict__ rstd, int M, int D, float eps,
+                                   const LayerHeader* hdr, uint32_t expect_layer, uint32_t* err) {
+    if (hdr && blockIdx.x == 0 && threadIdx.x == 0) {
+        if (hdr->magic != kImageMagic || hdr->layer != expect_layer)
+            atomicCAS(err, 0u, (kDevErrTag << 24) | (expect_layer & 0xFFFFFFu));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (row >= M) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)row * D);
+    float ss = 0.f;
+    for (int c = lane; c < D / 8; c += 32) {
+        const uint4 v = xr[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf_lo(w[j]), b = bf_hi(w[j]);
+            ss = __fadd_rn(ss, __fmul_rn(a, a));
+            ss = __fadd_rn(ss, __fmul_rn(b, b));
+        }
+    }
+    ss = warp_sum_bcast(ss);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), eps)));
+    if (lane == 0) rstd[row] = r;
+    uint4* hr = reinterpret_cast<uint4*>(h + (int64_t)row * D);
+    for (int c = lane; c < D / 8; c += 32) {
+        const uint4 v = xr[c];
+        uint4 o;
+        o.x = bf2(__fmul_rn(bf_lo(v.x), r), __fmul_rn(bf_hi(v.x), r));
+        o.y = bf2(__fmul_rn(bf_lo(v.y), r), __fmul_rn(bf_hi(v.y), r));
+        o.z = bf2(__fmul_rn(bf_lo(v.z), r), __fmul_rn(bf_hi(v.z), r));
+        o.w = bf2(__fmul_rn(bf_lo(v.w), r), __fmul_rn(bf_hi(v.w), r));
+        hr[c] = o;
+    }
+}
+
+// dx = dx_next + rstd*dh - rstd^3 * x * mean(dh * x); also writes a bf16 copy of dx.
+__global__ void rmsnorm_bwd_kernel(const uint16_t* __restrict__ x, const float* __restrict__ rstd,
+                                   const float* __restrict__ dh, float* __restrict__ dx,
+                                   uint16_t* __restrict__ dx_bf, int M, int D) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (row >= M) return;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)row * D);
+    const float4* dr = reinterpret_cast<const float4*>(dh + (int64_t)row * D);
+    float dot = 0.f;
+    for (int c = lane; c < D / 8; c += 32) {
+        const uint4 v = xr[c];
+        const float4 d0 = dr[2 * c], d1 = dr[2 * c + 1];
+        dot = __fadd_rn(dot, __fmul_rn(d0.x, bf_lo(v.x)));
+        dot = __fadd_rn(dot, __fmul_rn(d0.y, bf_hi(v.x)));
+        dot = __fadd_rn(dot, __fmul_rn(d0.z, bf_lo(v.y)));
+        dot = __fadd_rn(dot, __fmul_rn(d0.w, bf_hi(v.y)));
+        dot = __fadd_rn(dot, __fmul_rn(d1.x, bf_lo(v.z)));
+        dot = __fadd_rn(dot, __fmul_rn(d1.y, bf_hi(v.z)));
+        dot = __fadd_rn(dot, __fmul_rn(d1.z, bf_lo(v.w)));
+        dot = __fadd_rn(dot, __fmul_rn(d1.w, bf_hi(v.w)));
+    }
+    dot = warp_sum_bcast(dot);
+    const float r = rstd[row];
+    const float c3 = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), __fdiv_rn(dot, (float)D));
+    float4* xo = reinterpret_cast<float4*>(dx + (int64_t)row * D);
+    uint4* bo = reinterpret_cast<uint4*>(dx_bf + (int64_t)row * D);
+    for (int c = lane; c < D / 8; c += 32) {
+        const uint4 v = xr[c];
+        const float4 d0 = dr[2 * c], d1 = dr[2 * c + 1];
+        float4 g0 = xo[2 * c], g1 = xo[2 * c + 1];
+        const float xs[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
+                             bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
+        const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        float gs[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            gs[j] = __fsub_rn(__fadd_rn(gs[j], __fmul_rn(r, ds[j])), __fmul_rn(c3, xs[j]));
+        xo[2 * c] = make_float4(gs[0], gs[1], gs[2], gs[3]);
+        xo[2 * c + 1] = make_float4(gs[4], gs[5], gs[6], gs[7]);
+        bo[c] = make_uint4(bf2(gs[0], gs[1]), bf2(gs[2], gs[3]), bf2(gs[4], gs[5]), bf2(gs[6], gs[7]));
+    }
+}
+
+// --------------------------------------------------------------------------- SiLU-mul
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+// a = bf16(silu(g) * u); g, u are column blocks of the fused projection output.
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ y, int64_t ldy, int og, int ou,
+                                uint16_t* __restrict__ a, int M, int F) {
+    const int64_t chunks = (int64_t)M * (F / 8);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / (F / 8);
+        const int c = (int)(i - row * (F / 8)) * 8;
+        const uint4 g = *reinterpret_cast<const uint4*>(y + row * ldy + og + c);
+        const uint4 u = *reinterpret_cast<const uint4*>(y + row * ldy + ou + c);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = bf2(__fmul_rn(silu_f(bf_lo(gw[j])), bf_lo(uw[j])),
+                       __fmul_rn(silu_f(bf_hi(gw[j])), bf_hi(uw[j])));
+        *reinterpret_cast<uint4*>(a + row * F + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ------------------------------------------------------------------ loss and seeds
+
+// Per-block sums of k^2 and v^2 over rows blockIdx.x, blockIdx.x + kLossBlocks, ...
+__global__ void kv_sumsq_kernel(const uint16_t* __restrict__ y, int64_t ldy, int ok, int ov, int dkv,
+                                int M, float* __restrict__ part) {
+    __shared__ float sh[256];
+    float sk = 0.f, sv = 0.f;
+    for (int row = blockIdx.x; row < M; row += gridDim.x) {
+        for (int c = threadIdx.x * 8; c < dkv; c += 256 * 8) {
+            const uint4 k = *reinterpret_cast<const uint4*>(y + (int64_t)row * ldy + ok + c);
+            const uint4 v = *reinterpret_cast<const uint4*>(y + (int64_t)row * ldy + ov + c);
+            const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sk = __fadd_rn(sk, __fmul_rn(bf_lo(kw[j]), bf_lo(kw[j])));
+                sk = __fadd_rn(sk, __fmul_rn(bf_hi(kw[j]), bf_hi(kw[j])));
+                sv = __fadd_rn(sv, __fmul_rn(bf_lo(vw[j]), bf_lo(vw[j])));
+                sv = __fadd_rn(sv, __fmul_rn(bf_hi(vw[j]), bf_hi(vw[j])));
+            }
+        }
+    }
+    const float tk = block_sum256(sk, sh);
+    __syncthreads();
+    const float tv = block_sum256(sv, sh);
+    if (threadIdx.x == 0) {
+        part[2 * blockIdx.x] = tk;
+        part[2 * blockIdx.x + 1] = tv;
+    }
+}
+
+// Seed gradient dx = x / (M*D) (fp32 and bf16) and per-block sums of x^2.
+__global__ void loss_seed_kernel(const uint16_t* __restrict__ x, int M, int D, float inv_md,
+                                 float* __restrict__ dx, uint16_t* __restrict__ dx_bf,
+                                 float* __restrict__ part) {
+    __shared__ float sh[256];
+    float s = 0.f;
+    for (int row = blockIdx.x; row < M; row += gridDim.x) {
+        for (int c = threadIdx.x * 8; c < D; c += 256 * 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(x + (int64_t)row * D + c);
+            const float xs[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
+                                 bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
+            float g[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                s = __fadd_rn(s, __fmul_rn(xs[j], xs[j]));
+                g[j] = __fmul_rn(xs[j], inv_md);
+            }
+            float4* o = reinterpret_cast<float4*>(dx + (int64_t)row * D + c);
+            o[0] = make_float4(g[0], g[1], g[2], g[3]);
+            o[1] = make_float4(g[4], g[5], g[6], g[7]);
+            *reinterpret_cast<uint4*>(dx_bf + (int64_t)row * D + c) =
+                make_uint4(bf2(g[0], g[1]), bf2(g[2], g[3]), bf2(g[4], g[5]), bf2(g[6], g[7]));
+        }
+    }
+    const float t = block_sum256(s, sh);
+    if (threadIdx.x == 0) part[blockIdx.x] = t;
+}
+
+// loss = 0.5 * Sx / (M D) + sum_l coef (Sk_l + Sv_l) / (M dkv), summed in a fixed order in fp64.
+__global__ void loss_final_kernel(const float* __restrict__ xpart, const float* __restrict__ kvpart,
+                                  int n_layers, int nb, double inv_md, double coef_inv_mkv,
+                                  float* __restrict__ loss) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    double sx = 0.0;
+    for (int b = 0; b < nb; ++b) sx += (double)xpart[b];
+    double l = 0.5 * sx * inv_md;
+    for (int layer = 0; layer < n_layers; ++layer) {
+        double skv = 0.0;
+        for (int b = 0; b < nb; ++b)
+            skv += (double)kvpart[(size_t)layer * nb * 2 + 2 * b] + (double)kvpart[(size_t)layer * nb * 2 + 2 * b + 1];
+        l += coef_inv_mkv * skv;
+    }
+    *loss = (float)l;
+}
+
+// ------------------------------------------------------------- backward dY assembly
+
+// dY_cat = [dq | dk | dv | dgate | dup] (bf16) from dqa = [dq | da] (fp32), the forward
+// outputs (k, v, gate, up) and the k/v loss coefficient.
+__global__ void dy_build_kernel(const float* __restrict__ dqa, const uint16_t* __restrict__ y,
+                                uint16_t* __restrict__ dy, int M, int D, int dkv, int F, float kv_coef) {
+    const int ldq = D + F;
+    const int ldy = D + 2 * dkv + 2 * F;
+    const int ok = D, ov = D + dkv, og = D + 2 * dkv, ou = og + F;
+    const int per_row = D / 8 + (2 * dkv) / 8 + F / 8;
+    const int64_t total = (int64_t)M * per_row;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = i / per_row;
+        int c = (int)(i - row * per_row) * 8;
+        const float* dr = dqa + row * ldq;
+        const uint16_t* yr = y + row * ldy;
+        uint16_t* orow = dy + row * ldy;
+        if (c < D) {
+            const float4 a0 = *reinterpret_cast<const float4*>(dr + c);
+            const float4 a1 = *reinterpret_cast<const float4*>(dr + c + 4);
+            *reinterpret_cast<uint4*>(orow + c) =
+                make_uint4(bf2(a0.x, a0.y), bf2(a0.z, a0.w), bf2(a1.x, a1.y), bf2(a1.z, a1.w));
+            continue;
+        }
+        c -= D;
+        if (c < 2 * dkv) {
+            const int col = ok + c;   // k block then v block are adjacent
+            const uint4 v = *reinterpret_cast<const uint4*>(yr + col);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = bf2(__fmul_rn(kv_coef, bf_lo(w[j])), __fmul_rn(kv_coef, bf_hi(w[j])));
+            *reinterpret_cast<uint4*>(orow + col) = make_uint4(o[0], o[1], o[2], o[3]);
+            continue;
+        }
+        c -= 2 * dkv;
+        const float4 a0 = *reinterpret_cast<const float4*>(dr + D + c);
+        const float4 a1 = *reinterpret_cast<const float4*>(dr + D + c + 4);
+        const float da[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint4 g4 = *reinterpret_cast<const uint4*>(yr + og + c);
+        const uint4 u4 = *reinterpret_cast<const uint4*>(yr + ou + c);
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+        float dg[8], du[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float gg[2] = {bf_lo(gw[j]), bf_hi(gw[j])};
+            const float uu[2] = {bf_lo(uw[j]), bf_hi(uw[j])};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float g = gg[e];
+                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+                const float d = da[2 * j + e];
+                // dg = da * u * sig(g) * (1 + g (1 - sig(g))),  du = da * g * sig(g)
+                const float t = __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg)));
+                dg[2 * j + e] = __fmul_rn(__fmul_rn(__fmul_rn(d, uu[e]), sg), t);
+                du[2 * j + e] = __fmul_rn(__fmul_rn(d, g), sg);
+            }
+        }
+        *reinterpret_cast<uint4*>(orow + og + c) =
+            make_uint4(bf2(dg[0], dg[1]), bf2(dg[2], dg[3]), bf2(dg[4], dg[5]), bf2(dg[6], dg[7]));
+        *reinterpret_cast<uint4*>(orow + ou + c) =
+            make_uint4(bf2(du[0], du[1]), bf2(du[2], du[3]), bf2(du[4], du[5]), bf2(du[6], du[7]));
+    }
+}
+
+// ---------------------------------------------------------------------- launchers
+
+static inline unsigned grid_for(int64_t work, int per_block) {
+    int64_t b = (work + per_block - 1) / per_block;
+    if (b < 1) b = 1;
+    if (b > 148 * 16) b = 148 * 16;
+    return (unsigned)b;
+}
+
+int launch_rmsnorm_fwd(const uint16_t* x, uint16_t* h, float* rstd, int M, int D, float eps,
+                       const void* header, uint32_t layer, cudaStream_t s) {
+    uint32_t* err = header ? device_error_word() : nullptr;
+    if (header && !err) return LSN_ECUDA;
+    rmsnorm_fwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, h, rstd, M, D, eps,
+                                                   static_cast<const LayerHeader*>(header), layer, err);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_tag_check(const void* header, uint32_t layer, cudaStream_t s) {
+    uint32_t* err = device_error_word();
+    if (!err) return LSN_ECUDA;
+    tag_check_kernel<<<1, 32, 0, s>>>(static_cast<const LayerHeader*>(header), layer, err);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_rmsnorm_bwd(const uint16_t* x, const float* rstd, const float* dh, float* dx, uint16_t* dx_bf,
+                       int M, int D, cudaStream_t s) {
+    rmsnorm_bwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, rstd, dh, dx, dx_bf, M, D);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_silu_mul(const uint16_t* y, int64_t ldy, int og, int ou, uint16_t* a, int M, int F, cudaStream_t s) {
+    silu_mul_kernel<<<grid_for((int64_t)M * F / 8, 256), 256, 0, s>>>(y, ldy, og, ou, a, M, F);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_kv_sumsq(const uint16_t* y, int64_t ldy, int ok, int ov, int dkv, int M, float* part, cudaStream_t s) {
+    kv_sumsq_kernel<<<kLossBlocks, 256, 0, s>>>(y, ldy, ok, ov, dkv, M, part);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv_coef, float* dx, uint16_t* dx_bf,
+                float* xpart, const float* kvpart, float* loss, cudaStream_t s) {
+    const double md = (double)M * (double)D;
+    loss_seed_kernel<<<kLossBlocks, 256, 0, s>>>(x, M, D, (float)(1.0 / md), dx, dx_bf, xpart);
+    LSN_CUDA_TRY(cudaGetLastError());
+    loss_final_kernel<<<1, 32, 0, s>>>(xpart, kvpart, n_layers, kLossBlocks, 1.0 / md,
+                                       (double)kv_coef / ((double)M * (double)dkv), loss);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
+                    float kv_coef, cudaStream_t s) {
+    const int64_t work = (int64_t)M * (D / 8 + 2 * dkv / 8 + F / 8);
+    dy_build_kernel<<<grid_for(work, 256), 256, 0, s>>>(dqa, y, dy, M, D, dkv, F, kv_coef);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+}  // namespace lsn

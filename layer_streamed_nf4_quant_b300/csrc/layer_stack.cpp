@@ -1,0 +1,418 @@
+// layer_stack_step: the forward sweep, the loss and the reverse backward sweep over the
+// synthetic decoder-layer stack, with every layer's packed weights coming through the
+// two-slot stream pool (or from a resident device store).
+//
+// "Can You Fine-Tune Llama 3.1 8B on a 4GB GPU? Soup's Layer Streaming Explained":
+//   section "How Soup's layer streaming actually works" -- one layer at a time in reusable
+//   VRAM buffers, the next prefetched while the current computes, every layer read again in
+//   the backward pass;
+//   section "The gradient bug also reveals something important about AI benchmarks" -- the
+//   streamed run must give the resident run's forward output and LoRA gradients.
+// Both modes below enqueue the same kernels with the same arguments except the weight
+// addresses, and no kernel's arithmetic depends on an address, so they agree bit for bit.
+//
+// Per layer (s = alpha / r, canonical projection order q, k, v, gate, up, o, down):
+//   forward : h = rmsnorm(x); T_cat = h A_cat^T; [q|k|v|g|u] = h W_p^T + s T_p B_p^T;
+//             a = silu(g) u; T_od = [q A_o^T | a A_d^T]; x' = x + [q|a][W_o|W_d]^T + s T_od [B_o|B_d]^T
+//   backward: dT_od = s dx' [B_o|B_d]; dB_o,d; dA_o,d; [dq|da] = dx' [W_o|W_d] + dT_od [A_o;A_d];
+//             dY_cat = [dq | dk | dv | dg | du]; dT_cat = s dY_p B_p; dB_p; dA_p;
+//             dh = sum_p dY_p W_p + dT_cat A_cat;  dx = dx' + rmsnorm'(dh)
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "lsn_internal.h"
+#include "stack_kernels.h"
+#include "tc_gemm.h"
+
+using namespace lsn;
+
+namespace {
+
+inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
+inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+inline int tiles_of(int64_t m, int64_t n, int bn) { return ceil_div(m, kBM) * ceil_div(n, bn); }
+
+struct Dims {
+    int L, D, dkv, F, r, M, Ncat;
+    float s, eps, coef;
+    int np[kNumProj];   // n_out per projection
+    int kp[kNumProj];   // k_in per projection
+    int coff[5];        // column offset of q, k, v, gate, up in the fused output
+};
+
+struct Buffers {
+    std::vector<uint16_t*> x;    // L+1 (x[0] = caller's x0)
+    std::vector<uint16_t*> h, y, a, tcat, tod;
+    std::vector<float*> rstd;
+    float* dx = nullptr;
+    uint16_t* dx_bf = nullptr;
+    uint16_t* dtod = nullptr;
+    float* dqa = nullptr;
+    uint16_t* dy = nullptr;
+    uint16_t* dtcat = nullptr;
+    float* dh = nullptr;
+    float* kvpart = nullptr;
+    float* xpart = nullptr;
+    float* partial = nullptr;
+    size_t partial_bytes = 0;
+};
+
+bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
+    if (!d || d->n_layers < 1 || d->d_model < 256 || d->d_model % 256 || d->d_kv < 256 || d->d_kv % 256 ||
+        d->d_ff < 256 || d->d_ff % 256 || d->rank < 8 || d->rank > 64 || d->rank % 8 || M < 1 ||
+        M > (1 << 24))
+        return false;
+    o->L = d->n_layers;
+    o->D = d->d_model;
+    o->dkv = d->d_kv;
+    o->F = d->d_ff;
+    o->r = d->rank;
+    o->M = (int)M;
+    o->Ncat = o->D + 2 * o->dkv + 2 * o->F;
+    o->s = d->lora_alpha / (float)d->rank;
+    o->eps = d->rms_eps;
+    o->coef = d->kv_loss_coef;
+    for (int p = 0; p < kNumProj; ++p) {
+        int64_t n, k;
+        proj_shape(d, p, &n, &k);
+        o->np[p] = (int)n;
+        o->kp[p] = (int)k;
+    }
+    o->coff[0] = 0;
+    o->coff[1] = o->D;
+    o->coff[2] = o->D + o->dkv;
+    o->coff[3] = o->D + 2 * o->dkv;
+    o->coff[4] = o->D + 2 * o->dkv + o->F;
+    return true;
+}
+
+// Lays the activations and scratch out in ws (base == nullptr: only sizes).  Returns bytes.
+size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size_t partial_bytes) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> uint8_t* {
+        uint8_t* p = base ? base + off : nullptr;
+        off += a256(bytes);
+        return p;
+    };
+    const size_t M = (size_t)d.M;
+    b->x.assign(d.L + 1, nullptr);
+    b->h.assign(d.L, nullptr);
+    b->y.assign(d.L, nullptr);
+    b->a.assign(d.L, nullptr);
+    b->tcat.assign(d.L, nullptr);
+    b->tod.assign(d.L, nullptr);
+    b->rstd.assign(d.L, nullptr);
+    b->x[0] = const_cast<uint16_t*>(x0);
+    for (int l = 0; l < d.L; ++l) {
+        b->x[l + 1] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        b->h[l] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        b->rstd[l] = reinterpret_cast<float*>(take(M * 4));
+        b->y[l] = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
+        b->a[l] = reinterpret_cast<uint16_t*>(take(M * d.F * 2));
+        b->tcat[l] = reinterpret_cast<uint16_t*>(take(M * 5 * d.r * 2));
+        b->tod[l] = reinterpret_cast<uint16_t*>(take(M * 2 * d.r * 2));
+    }
+    b->dx = reinterpret_cast<float*>(take(M * d.D * 4));
+    b->dx_bf = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+    b->dtod = reinterpret_cast<uint16_t*>(take(M * 2 * d.r * 2));
+    b->dqa = reinterpret_cast<float*>(take(M * (d.D + d.F) * 4));
+    b->dy = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
+    b->dtcat = reinterpret_cast<uint16_t*>(take(M * 5 * d.r * 2));
+    b->dh = reinterpret_cast<float*>(take(M * d.D * 4));
+    b->kvpart = reinterpret_cast<float*>(take((size_t)d.L * kLossBlocks * 2 * 4));
+    b->xpart = reinterpret_cast<float*>(take((size_t)kLossBlocks * 4));
+    b->partial = reinterpret_cast<float*>(take(partial_bytes));
+    b->partial_bytes = partial_bytes;
+    return off;
+}
+
+struct Ctx {
+    Dims d;
+    Buffers b;
+    cudaStream_t s = nullptr;
+    bool dry = false;
+    size_t partial_need = 0;
+    size_t img_off[kNumProj];
+    size_t la[kNumProj], lb[kNumProj];   // LoRA element offsets (A_p, B_p)
+
+    int run(GemmPlan& g) {
+        if (g.status()) return g.status();
+        if (dry) {
+            partial_need = std::max(partial_need, g.partial_bytes());
+            return LSN_OK;
+        }
+        return g.launch(s, b.partial, b.partial_bytes);
+    }
+    const void* mat(const uint8_t* img, int p) const { return img ? img + img_off[p] : nullptr; }
+    const uint16_t* A(const uint16_t* lo, int p) const { return lo ? lo + la[p] : nullptr; }
+    const uint16_t* B(const uint16_t* lo, int p) const { return lo ? lo + lb[p] : nullptr; }
+    float* dA(float* g, int p) const { return g ? g + la[p] : nullptr; }
+    float* dB(float* g, int p) const { return g ? g + lb[p] : nullptr; }
+};
+
+#define RC(x)                    \
+    do {                         \
+        int rc_ = (x);           \
+        if (rc_) return rc_;     \
+    } while (0)
+
+// --------------------------------------------------------------------------- forward
+
+int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora) {
+    const Dims& d = c.d;
+    const Buffers& b = c.b;
+    const int M = d.M, D = d.D, r = d.r;
+    if (!c.dry) RC(launch_rmsnorm_fwd(b.x[l], b.h[l], b.rstd[l], M, D, d.eps, img, (uint32_t)l, c.s));
+    {   // T_cat = bf16(h A_cat^T)
+        GemmPlan g(c.dry);
+        int mh = g.map(b.h[l], M, D, D, kBM);
+        int ma = g.map(c.A(lora, kQ), 5 * r, D, D, 64);
+        g.problem(M, 5 * r, 64, A_KMAJOR, EPI_BF16, b.tcat[l], 5 * r, 1.0f, 5 * r,
+                  choose_splits(tiles_of(M, 5 * r, 64), D / kBK));
+        g.seg(mh, 0, B_TMA_K, ma, 0, 0, D);
+        RC(c.run(g));
+    }
+    {   // q, k, v, gate, up = bf16(h W_p^T + s T_p B_p^T)
+        GemmPlan g(c.dry);
+        int mh = g.map(b.h[l], M, D, D, kBM);
+        int mt = g.map(b.tcat[l], M, 5 * r, 5 * r, kBM);
+        int tiles = 0;
+        for (int p = 0; p < 5; ++p) tiles += tiles_of(M, d.np[p], 256);
+        const int sp = choose_splits(tiles, D / kBK + 1);
+        for (int p = 0; p < 5; ++p) {
+            int v = g.nf4(c.mat(img, p), d.np[p], D);
+            g.problem(M, d.np[p], 256, A_KMAJOR, EPI_BF16, b.y[l] ? b.y[l] + d.coff[p] : nullptr, d.Ncat, 1.0f,
+                      d.np[p], sp);
+            g.seg(mh, 0, B_NF4_K, v, 0, 0, D);
+            g.seg_scaled(mt, p * r, c.B(lora, p), r, d.np[p], r, d.s);
+        }
+        RC(c.run(g));
+    }
+    if (!c.dry) RC(launch_silu_mul(b.y[l], d.Ncat, d.coff[3], d.coff[4], b.a[l], M, d.F, c.s));
+    {   // T_o = bf16(q A_o^T), T_d = bf16(a A_d^T)
+        GemmPlan g(c.dry);
+        int mq = g.map(b.y[l], M, D, d.Ncat, kBM);
+        int ma = g.map(b.a[l], M, d.F, d.F, kBM);
+        int mao = g.map(c.A(lora, kO), r, D, D, 64);
+        int mad = g.map(c.A(lora, kDown), r, d.F, d.F, 64);
+        const int tiles = 2 * tiles_of(M, r, 64);
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l], 2 * r, 1.0f, r, choose_splits(tiles, D / kBK));
+        g.seg(mq, 0, B_TMA_K, mao, 0, 0, D);
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l] ? b.tod[l] + r : nullptr, 2 * r, 1.0f, r,
+                  choose_splits(tiles, d.F / kBK));
+        g.seg(ma, 0, B_TMA_K, mad, 0, 0, d.F);
+        RC(c.run(g));
+    }
+    {   // x' = bf16(x + q W_o^T + a W_d^T + s T_o B_o^T + s T_d B_d^T)
+        GemmPlan g(c.dry);
+        int mq = g.map(b.y[l], M, D, d.Ncat, kBM);
+        int ma = g.map(b.a[l], M, d.F, d.F, kBM);
+        int mt = g.map(b.tod[l], M, 2 * r, 2 * r, kBM);
+        int vo = g.nf4(c.mat(img, kO), D, D);
+        int vd = g.nf4(c.mat(img, kDown), D, d.F);
+        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, b.x[l + 1], D, 1.0f, D,
+                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK + 2), b.x[l], D);
+        g.seg(mq, 0, B_NF4_K, vo, 0, 0, D);
+        g.seg(ma, 0, B_NF4_K, vd, 0, 0, d.F);
+        g.seg_scaled(mt, 0, c.B(lora, kO), r, D, r, d.s);
+        g.seg_scaled(mt, r, c.B(lora, kDown), r, D, r, d.s);
+        RC(c.run(g));
+    }
+    if (!c.dry)
+        RC(launch_kv_sumsq(b.y[l], d.Ncat, d.coff[1], d.coff[2], d.dkv, M, b.kvpart + (size_t)l * kLossBlocks * 2, c.s));
+    return LSN_OK;
+}
+
+// -------------------------------------------------------------------------- backward
+
+int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* grad) {
+    const Dims& d = c.d;
+    const Buffers& b = c.b;
+    const int M = d.M, D = d.D, F = d.F, r = d.r;
+    if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
+    {   // dT_o = bf16(s dx' B_o), dT_d = bf16(s dx' B_d)
+        GemmPlan g(c.dry);
+        int mdx = g.map(b.dx_bf, M, D, D, kBM);
+        int mbo = g.map(c.B(lora, kO), D, r, r, 64);
+        int mbd = g.map(c.B(lora, kDown), D, r, r, 64);
+        const int sp = choose_splits(2 * tiles_of(M, r, 64), D / kBK);
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtod, 2 * r, d.s, r, sp);
+        g.seg(mdx, 0, B_TMA_MN, mbo, 0, 0, D);
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtod ? b.dtod + r : nullptr, 2 * r, d.s, r, sp);
+        g.seg(mdx, 0, B_TMA_MN, mbd, 0, 0, D);
+        RC(c.run(g));
+    }
+    {   // dB_o, dB_d, dA_o, dA_d and [dq | da] = dx' [W_o | W_d] + dT_od [A_o ; A_d]
+        GemmPlan g(c.dry);
+        int mdx_mn = g.map(b.dx_bf, M, D, D, 64);
+        int mtod_mn = g.map(b.tod[l], M, 2 * r, 2 * r, 64);
+        int mq_mn = g.map(b.y[l], M, D, d.Ncat, 64);
+        int ma_mn = g.map(b.a[l], M, F, F, 64);
+        int mdtod_mn = g.map(b.dtod, M, 2 * r, 2 * r, 64);
+        int mdx = g.map(b.dx_bf, M, D, D, kBM);
+        int mdtod = g.map(b.dtod, M, 2 * r, 2 * r, kBM);
+        int mao = g.map(c.A(lora, kO), r, D, D, 64);
+        int mad = g.map(c.A(lora, kDown), r, F, F, 64);
+        int vo = g.nf4(c.mat(img, kO), D, D);
+        int vd = g.nf4(c.mat(img, kDown), D, F);
+        const int tiles = 3 * tiles_of(D, r, 64) + tiles_of(F, r, 64) + tiles_of(M, D, 256) + tiles_of(M, F, 256);
+        const int ws = choose_splits(tiles, ceil_div(M, kBK));
+        const int xs = choose_splits(tiles, D / kBK + 1);
+        g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kO), r, d.s, r, ws);
+        g.seg(mdx_mn, 0, B_TMA_MN, mtod_mn, 0, 0, M);
+        g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kDown), r, d.s, r, ws);
+        g.seg(mdx_mn, 0, B_TMA_MN, mtod_mn, 0, r, M);
+        g.problem(D, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, kO), D, 1.0f, r, ws);
+        g.seg(mq_mn, 0, B_TMA_MN, mdtod_mn, 0, 0, M);
+        g.problem(F, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, kDown), F, 1.0f, r, ws);
+        g.seg(ma_mn, 0, B_TMA_MN, mdtod_mn, 0, r, M);
+        g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dqa, D + F, 1.0f, D, xs);
+        g.seg(mdx, 0, B_NF4_MN, vo, 0, 0, D);
+        g.seg(mdtod, 0, B_TMA_MN, mao, 0, 0, r);
+        g.problem(M, F, 256, A_KMAJOR, EPI_F32, b.dqa ? b.dqa + D : nullptr, D + F, 1.0f, F, xs);
+        g.seg(mdx, 0, B_NF4_MN, vd, 0, 0, D);
+        g.seg(mdtod, r, B_TMA_MN, mad, 0, 0, r);
+        RC(c.run(g));
+    }
+    if (!c.dry)
+        RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / ((double)M * d.dkv)), c.s));
+    {   // dT_p = bf16(s dY_p B_p)
+        GemmPlan g(c.dry);
+        int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
+        int tiles = 5 * tiles_of(M, r, 64);
+        for (int p = 0; p < 5; ++p) {
+            int mb = g.map(c.B(lora, p), d.np[p], r, r, 64);
+            g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtcat ? b.dtcat + p * r : nullptr, 5 * r, d.s, r,
+                      choose_splits(tiles, ceil_div(d.np[p], kBK)));
+            g.seg(mdy, d.coff[p], B_TMA_MN, mb, 0, 0, d.np[p]);
+        }
+        RC(c.run(g));
+    }
+    {   // dB_p, dA_p and dh = sum_p dY_p W_p + dT_cat A_cat
+        GemmPlan g(c.dry);
+        int mdyp[5];
+        for (int p = 0; p < 5; ++p) mdyp[p] = g.map(b.dy ? b.dy + d.coff[p] : nullptr, M, d.np[p], d.Ncat, 64);
+        int mtcat_mn = g.map(b.tcat[l], M, 5 * r, 5 * r, 64);
+        int mh_mn = g.map(b.h[l], M, D, D, 64);
+        int mdtcat_mn = g.map(b.dtcat, M, 5 * r, 5 * r, 64);
+        int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
+        int mdtcat = g.map(b.dtcat, M, 5 * r, 5 * r, kBM);
+        int macat = g.map(c.A(lora, kQ), 5 * r, D, D, 64);
+        int tiles = 5 * tiles_of(D, r, 64) + tiles_of(M, D, 256);
+        for (int p = 0; p < 5; ++p) tiles += tiles_of(d.np[p], r, 64);
+        const int ws = choose_splits(tiles, ceil_div(M, kBK));
+        for (int p = 0; p < 5; ++p) {
+            g.problem(d.np[p], r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, p), r, d.s, r, ws);
+            g.seg(mdyp[p], 0, B_TMA_MN, mtcat_mn, 0, p * r, M);
+        }
+        for (int p = 0; p < 5; ++p) {
+            g.problem(D, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, p), D, 1.0f, r, ws);
+            g.seg(mh_mn, 0, B_TMA_MN, mdtcat_mn, 0, p * r, M);
+        }
+        int ksteps = 1;
+        for (int p = 0; p < 5; ++p) ksteps += ceil_div(d.np[p], kBK);
+        g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dh, D, 1.0f, D, choose_splits(tiles, ksteps));
+        for (int p = 0; p < 5; ++p) {
+            int v = g.nf4(c.mat(img, p), d.np[p], D);
+            g.seg(mdy, d.coff[p], B_NF4_MN, v, 0, 0, d.np[p]);
+        }
+        g.seg(mdtcat, 0, B_TMA_MN, macat, 0, 0, 5 * r);
+        RC(c.run(g));
+    }
+    if (!c.dry) RC(launch_rmsnorm_bwd(b.x[l], b.rstd[l], b.dh, b.dx, b.dx_bf, M, D, c.s));
+    return LSN_OK;
+}
+
+int init_ctx(Ctx& c, const lsn_stack_desc* desc, int64_t M) {
+    if (!make_dims(desc, M, &c.d)) return fail(LSN_EINVAL, "layer stack: bad descriptor or M");
+    RC(lsn_layer_image_offsets(desc, c.img_off));
+    size_t lo[2 * kNumProj];
+    RC(lsn_lora_offsets(desc, lo));
+    for (int p = 0; p < kNumProj; ++p) {
+        c.la[p] = lo[p];
+        c.lb[p] = lo[kNumProj + p];
+    }
+    return LSN_OK;
+}
+
+size_t partial_need(const lsn_stack_desc* desc, int64_t M) {
+    Ctx c;
+    if (init_ctx(c, desc, M)) return 0;
+    c.dry = true;
+    layout(c.d, nullptr, nullptr, &c.b, 0);
+    if (fwd_layer(c, 0, nullptr, nullptr) || bwd_layer(c, 0, nullptr, nullptr, nullptr)) return 0;
+    return c.partial_need;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lsn_stack_workspace_bytes(const lsn_stack_desc* desc, int64_t M) {
+    Ctx c;
+    if (init_ctx(c, desc, M)) return 0;
+    Buffers b;
+    return layout(c.d, nullptr, nullptr, &b, partial_need(desc, M)) + 256;
+}
+
+int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack_desc* desc, const uint16_t* x0,
+                     int64_t M, const uint16_t* const* lora, float* const* grads, float* loss_out, uint16_t* x_out,
+                     float* dx0, void* ws, size_t ws_bytes, void* stream) {
+    Ctx c;
+    RC(init_ctx(c, desc, M));
+    if (!x0 || !lora || !grads || !loss_out || !ws || (!pool && !resident_store))
+        return fail(LSN_EINVAL, "layer_stack_step: NULL argument");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) || (reinterpret_cast<uintptr_t>(x0) & 15))
+        return fail(LSN_EINVAL, "layer_stack_step: ws must be 256-byte and x0 16-byte aligned");
+    for (int l = 0; l < c.d.L; ++l)
+        if (!lora[l] || !grads[l] || (reinterpret_cast<uintptr_t>(lora[l]) & 15) ||
+            (reinterpret_cast<uintptr_t>(grads[l]) & 15))
+            return fail(LSN_EINVAL, "layer_stack_step: LoRA / grad blob %d missing or misaligned", l);
+    const size_t pneed = partial_need(desc, M);
+    const size_t need = layout(c.d, nullptr, nullptr, &c.b, pneed);
+    if (ws_bytes < need) return fail(LSN_ENOMEM, "layer_stack_step: workspace %zu < %zu", ws_bytes, need);
+    layout(c.d, static_cast<uint8_t*>(ws), x0, &c.b, pneed);
+    c.s = static_cast<cudaStream_t>(stream);
+    const size_t img_bytes = lsn_layer_image_bytes(desc);
+    const uint8_t* res = static_cast<const uint8_t*>(resident_store);
+    const int L = c.d.L;
+    auto image = [&](int l, const uint8_t** img) -> int {
+        if (!pool) {
+            *img = res + (size_t)l * img_bytes;
+            return LSN_OK;
+        }
+        const void* p = nullptr;
+        int rc = stream_pool_wait(pool, l, stream, &p, 0);
+        *img = static_cast<const uint8_t*>(p);
+        return rc;
+    };
+
+    // forward sweep, prefetching one layer ahead
+    if (pool) RC(stream_pool_prefetch(pool, 0));
+    for (int l = 0; l < L; ++l) {
+        if (pool && l + 1 < L) RC(stream_pool_prefetch(pool, l + 1));
+        const uint8_t* img;
+        RC(image(l, &img));
+        RC(fwd_layer(c, l, img, lora[l]));
+        if (pool) RC(stream_pool_release(pool, l, stream));
+    }
+    RC(launch_loss(c.b.x[L], c.d.M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart, loss_out,
+                   c.s));
+    // reverse sweep, re-streaming every layer
+    if (pool) RC(stream_pool_prefetch(pool, L - 1));
+    for (int l = L - 1; l >= 0; --l) {
+        if (pool && l - 1 >= 0) RC(stream_pool_prefetch(pool, l - 1));
+        const uint8_t* img;
+        RC(image(l, &img));
+        RC(bwd_layer(c, l, img, lora[l], grads[l]));
+        if (pool) RC(stream_pool_release(pool, l, stream));
+    }
+    if (x_out)
+        LSN_CUDA_TRY(cudaMemcpyAsync(x_out, c.b.x[L], (size_t)c.d.M * c.d.D * 2, cudaMemcpyDeviceToDevice, c.s));
+    if (dx0) LSN_CUDA_TRY(cudaMemcpyAsync(dx0, c.b.dx, (size_t)c.d.M * c.d.D * 4, cudaMemcpyDeviceToDevice, c.s));
+    return LSN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,31 @@
+// Launchers of the memory-bound layer kernels (internal interface).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lsn {
+
+constexpr int kLossBlocks = 128;   // fixed grid of the loss reductions (fixes their order)
+
+// h = bf16(x * rstd), rstd = (mean(x^2) + eps)^-1/2.  If header is non-null, block 0 also
+// checks the layer image tag against `layer` and records a mismatch in the error word.
+int launch_rmsnorm_fwd(const uint16_t* x, uint16_t* h, float* rstd, int M, int D, float eps,
+                       const void* header, uint32_t layer, cudaStream_t s);
+// Checks a layer image's tag (magic and layer index) and records a mismatch.
+int launch_tag_check(const void* header, uint32_t layer, cudaStream_t s);
+// dx += rstd*dh - rstd^3 * x * mean(dh*x)  (in place), dx_bf = bf16(dx).
+int launch_rmsnorm_bwd(const uint16_t* x, const float* rstd, const float* dh, float* dx, uint16_t* dx_bf,
+                       int M, int D, cudaStream_t s);
+// a = bf16(silu(y[:, og:og+F]) * y[:, ou:ou+F]).
+int launch_silu_mul(const uint16_t* y, int64_t ldy, int og, int ou, uint16_t* a, int M, int F, cudaStream_t s);
+// part[2b], part[2b+1] = block sums of k^2 and v^2 (kLossBlocks blocks).
+int launch_kv_sumsq(const uint16_t* y, int64_t ldy, int ok, int ov, int dkv, int M, float* part, cudaStream_t s);
+// dx = x/(M*D) (fp32 and bf16) and the scalar loss from x's and the layers' k/v sums.
+int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv_coef, float* dx, uint16_t* dx_bf,
+                float* xpart, const float* kvpart, float* loss, cudaStream_t s);
+// dY_cat = [dq | 2c k/(M dkv) | 2c v/(M dkv) | dgate | dup] in bf16.
+int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
+                    float kv_coef, cudaStream_t s);
+
+}  // namespace lsn

@@ -1,0 +1,783 @@
+// Grouped tcgen05 GEMM for sm_103a with the NF4 block-dequant stage fused into its operand
+// producer, plus the fixed-order split reduction and the test-only dequant kernel.
+//
+// The hot path of layer-streamed LoRA ("Can You Fine-Tune Llama 3.1 8B on a 4GB GPU? Soup's
+// Layer Streaming Explained", "How Soup's layer streaming actually works" and "Why NF4
+// matters so much"): the frozen NF4 base W is applied forward (y = x W^T) and transposed
+// backward (dX = dY W) once per layer while the layer sits in a streamed VRAM slot.  Here W
+// is decoded 64 weights (one absmax block) at a time by producer warps directly into the
+// 128-byte-swizzled shared-memory operand tiles that tcgen05.mma reads; bf16 W never exists
+// in HBM.  The LoRA branch enters as extra contraction steps of the same accumulator
+// (s*T*B^T forward, dT*A backward), so one fp32 TMEM accumulator holds the full result.
+//
+// CTA roles (512 threads, one CTA per SM, persistent over a static tile order):
+//   warp 0       TMA producer of A (and of dense B) tiles
+//   warp 1       TMEM allocator and single-thread UMMA issuer
+//   warps 4-7    epilogue: TMEM -> registers -> global
+//   warps 8-15   B producer: NF4 decode / scaled LoRA-B rows into shared memory
+// Every tile has a fixed K order and a fixed owner; split-K partials are reduced in split
+// order by gemm_reduce.  No atomics touch results, so every launch is bit-reproducible and
+// independent of where the weights live.
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "lsn_internal.h"
+#include "tc_gemm.h"
+#include "tc_ptx.cuh"
+
+namespace lsn {
+
+static_assert(sizeof(GemmParams) <= 32764, "kernel parameters must fit the 32 KB limit");
+
+constexpr int kDequantWarp0 = 8;
+constexpr int kDequantWarps = 8;
+constexpr int kEpiWarp0 = 4;
+constexpr size_t kGemmSmemBytes =
+    1024 + (size_t)kStages * (kStageABytes + kStageBBytes) + 8 * (2 * kStages + 2) + 128;
+
+// Wait-site ids recorded in the device error word when a bounded wait runs out.
+enum : uint32_t { kSiteEmptyTma = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4,
+                  kSiteEmptyDeq = 5 };
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo_elem, hi_elem);   // .x (low half) = first
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Decodes the 64 weights W[row][col0 .. col0+63] (exactly one absmax block) into 32 words of
+// packed bf16 pairs, element order preserved.  Each weight is bf16_rn(fp32(level * a')),
+// a' = fp32(fp32(q * scale) + offset).
+__device__ __forceinline__ void nf4_decode_block(const Nf4Dev& w, int64_t row, int64_t col0,
+                                                 const float* lv, uint32_t (&o)[32]) {
+    const int64_t e0 = row * w.k_in + col0;
+    const int64_t blk = e0 >> 6;
+    const uint4* src = reinterpret_cast<const uint4*>(w.codes + (e0 >> 1));
+    const uint4 c0 = __ldg(src);
+    const uint4 c1 = __ldg(src + 1);
+    const float q = (float)__ldg(w.absmax + blk);
+    const int64_t g = blk >> 8;
+    const float a = __fadd_rn(__fmul_rn(q, __ldg(w.scale + g)), __ldg(w.offset + g));
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t b = (wd[i] >> (8 * j)) & 0xFFu;
+            // weight 2k sits in the high nibble of byte k
+            o[4 * i + j] = pack_bf16x2(__fmul_rn(lv[b >> 4], a), __fmul_rn(lv[b & 15u], a));
+        }
+    }
+}
+
+__device__ __forceinline__ void smem_row_zero(uint32_t dst) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) st_shared_v4(dst + (ch << 4), 0u, 0u, 0u, 0u);
+}
+
+// Writes 32 words (64 bf16) as one 128-byte swizzled row: 16-byte chunk ch goes to chunk
+// position ch ^ swz, swz = row index within its 8-row (1024-byte) group.
+__device__ __forceinline__ void smem_row_store(uint32_t dst, uint32_t swz, const uint32_t (&o)[32]) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(dst + ((ch ^ swz) << 4), o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+}
+
+// One row of a dense bf16 matrix (k <= 64 elements, k % 8 == 0) times `scale`, zero padded.
+__device__ __forceinline__ void smem_row_scaled(uint32_t dst, uint32_t swz, const uint16_t* src,
+                                                int k, float scale) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (ch * 8 < k) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = __uint_as_float(in[j] << 16);
+                const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
+                o[j] = pack_bf16x2(__fmul_rn(lo, scale), __fmul_rn(hi, scale));
+            }
+        }
+        st_shared_v4(dst + ((ch ^ swz) << 4), o[0], o[1], o[2], o[3]);
+    }
+}
+
+struct TileInfo {
+    int prob, m0, n0, split, ks_begin, ks_end;
+    bool half1;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+    int pi = 0;
+    while (pi + 1 < p.n_probs && t >= p.probs[pi + 1].tile_begin) ++pi;
+    const Problem& pr = p.probs[pi];
+    const int l = t - pr.tile_begin;
+    const int per_split = pr.tiles_m * pr.tiles_n;
+    const int s = l / per_split;
+    const int r = l - s * per_split;
+    const int nt = r / pr.tiles_m;
+    const int mt = r - nt * pr.tiles_m;
+    TileInfo ti;
+    ti.prob = pi;
+    ti.m0 = mt * kBM;
+    ti.n0 = nt * pr.bn;
+    ti.split = s;
+    ti.ks_begin = (int)((int64_t)pr.ksteps * s / pr.splits);
+    ti.ks_end = (int)((int64_t)pr.ksteps * (s + 1) / pr.splits);
+    ti.half1 = ti.m0 + 128 < pr.m;
+    return ti;
+}
+
+// Maps a problem-level k-step to (segment index, k-step within the segment).
+__device__ __forceinline__ void locate(const GemmParams& p, const Problem& pr, int ks, int& seg,
+                                       int& kk) {
+    int s = pr.seg_begin;
+    int k = ks;
+    while (s + 1 < pr.seg_begin + pr.seg_count && k >= p.segs[s].ksteps) {
+        k -= p.segs[s].ksteps;
+        ++s;
+    }
+    seg = s;
+    kk = k;
+}
+
+__device__ __forceinline__ bool seg_b_mn(int b_src) { return b_src == B_NF4_MN || b_src == B_TMA_MN; }
+
+// ----------------------------------------------------------------------------- epilogue
+
+__device__ __forceinline__ void epilogue_store(const Problem& pr, int split, int row, int col0,
+                                               const float (&v)[32]) {
+    if (col0 >= pr.n_valid) return;
+    const float al = pr.alpha;
+    switch (pr.epi) {
+        case EPI_BF16: {
+            uint16_t* o = static_cast<uint16_t*>(pr.out) + (int64_t)row * pr.ldo + col0;
+            const uint16_t* rs = pr.residual ? pr.residual + (int64_t)row * pr.ldr + col0 : nullptr;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (col0 + 8 * g >= pr.n_valid) break;
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = v[8 * g + j] * al;
+                if (rs) {
+                    const uint4 r4 = *reinterpret_cast<const uint4*>(rs + 8 * g);
+                    const uint32_t rr[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        f[2 * j] += __uint_as_float(rr[j] << 16);
+                        f[2 * j + 1] += __uint_as_float(rr[j] & 0xFFFF0000u);
+                    }
+                }
+                uint4 w;
+                w.x = pack_bf16x2(f[0], f[1]);
+                w.y = pack_bf16x2(f[2], f[3]);
+                w.z = pack_bf16x2(f[4], f[5]);
+                w.w = pack_bf16x2(f[6], f[7]);
+                *reinterpret_cast<uint4*>(o + 8 * g) = w;
+            }
+            break;
+        }
+        case EPI_F32:
+        case EPI_F32_ACC:
+        case EPI_PARTIAL: {
+            float* o;
+            float a2 = al;
+            if (pr.epi == EPI_PARTIAL) {
+                o = static_cast<float*>(pr.out) + (int64_t)split * pr.part_stride +
+                    (int64_t)row * pr.ldo + col0;
+                a2 = 1.0f;
+            } else {
+                o = static_cast<float*>(pr.out) + (int64_t)row * pr.ldo + col0;
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                if (col0 + 4 * g >= pr.n_valid) break;
+                float4 x = make_float4(v[4 * g] * a2, v[4 * g + 1] * a2, v[4 * g + 2] * a2,
+                                       v[4 * g + 3] * a2);
+                if (pr.epi == EPI_F32_ACC) {
+                    const float4 y = *reinterpret_cast<const float4*>(o + 4 * g);
+                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                }
+                *reinterpret_cast<float4*>(o + 4 * g) = x;
+            }
+            break;
+        }
+        case EPI_F32_T: {
+            float* o = static_cast<float*>(pr.out);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < pr.n_valid) o[(int64_t)(col0 + j) * pr.ldo + row] = v[j] * al;
+            break;
+        }
+        default:
+            break;
+    }
+}
+
+// ------------------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + kStages * kStageABytes;
+    const uint32_t sBar = sB + kStages * kStageBBytes;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (kStages + s); };
+    const uint32_t acc_full = sBar + 8u * (2 * kStages);
+    const uint32_t acc_empty = acc_full + 8u;
+    uint8_t* const gmisc = gbase + (sBar - base) + 8 * (2 * kStages + 2);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc + 4);
+    float* const lv = reinterpret_cast<float*>(gmisc + 64);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(full_bar(s), 1 + kDequantWarps);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        ptx::mbar_init(acc_full, 1);
+        ptx::mbar_init(acc_empty, 128);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < 16) lv[threadIdx.x] = p.levels[threadIdx.x];
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                const Problem& pr = p.probs[ti.prob];
+                for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
+                    if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err,
+                                                kSiteEmptyTma))
+                        goto tma_done;
+                    int si, kk;
+                    locate(p, pr, ks, si, kk);
+                    const KSeg& sg = p.segs[si];
+                    const uint32_t bar = full_bar(stage);
+                    const uint32_t a_dst = sA + stage * kStageABytes;
+                    const uint32_t b_dst = sB + stage * kStageBBytes;
+                    uint32_t bytes = kStageABytes;
+                    if (sg.b_src == B_TMA_K || sg.b_src == B_TMA_MN) bytes += pr.bn * kBK * 2;
+                    ptx::mbar_arrive_expect_tx(bar, bytes);
+                    const int ak = sg.a_k0 + kk * kBK;
+                    if (pr.a_major == A_KMAJOR) {
+                        ptx::tma_load_2d(a_dst, &p.maps[sg.a_map], ak, ti.m0, bar);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kBM / 64; ++i)
+                            ptx::tma_load_2d(a_dst + i * 8192, &p.maps[sg.a_map], ti.m0 + 64 * i, ak, bar);
+                    }
+                    const int bk = sg.b_k0 + kk * kBK;
+                    if (sg.b_src == B_TMA_K) {
+                        ptx::tma_load_2d(b_dst, &p.maps[sg.b_idx], bk, sg.b_n0 + ti.n0, bar);
+                    } else if (sg.b_src == B_TMA_MN) {
+                        for (int i = 0; i < pr.bn / 64; ++i)
+                            ptx::tma_load_2d(b_dst + i * 8192, &p.maps[sg.b_idx], sg.b_n0 + ti.n0 + 64 * i,
+                                             bk, bar);
+                    }
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        tma_done:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ UMMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                const Problem& pr = p.probs[ti.prob];
+                if (!ptx::mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, p.err, kSiteAccEmpty))
+                    break;
+                ptx::tc_fence_after();
+                const bool a_mn = pr.a_major == A_MNMAJOR;
+                for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
+                    if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteFull))
+                        goto mma_done;
+                    ptx::tc_fence_after();
+                    int si, kk;
+                    locate(p, pr, ks, si, kk);
+                    const bool b_mn = seg_b_mn(p.segs[si].b_src);
+                    const uint32_t idesc = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, b_mn ? 1 : 0);
+                    const uint32_t a_base = sA + stage * kStageABytes;
+                    const uint32_t b_base = sB + stage * kStageBBytes;
+#pragma unroll
+                    for (int k4 = 0; k4 < kBK / 16; ++k4) {
+                        const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(b_base + k4 * 2048, 8192, 1024)
+                                                    : ptx::smem_desc_sw128(b_base + k4 * 32, 16, 1024);
+                        const uint32_t acc = (ks > ti.ks_begin || k4 > 0) ? 1u : 0u;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (h == 1 && !ti.half1) break;
+                            const uint32_t ab = a_base + h * (kStageABytes / 2);
+                            const uint64_t adesc = a_mn ? ptx::smem_desc_sw128(ab + k4 * 2048, 8192, 1024)
+                                                        : ptx::smem_desc_sw128(ab + k4 * 32, 16, 1024);
+                            ptx::umma_f16(tmem + (uint32_t)(h * pr.bn), adesc, bdesc, idesc, acc);
+                        }
+                    }
+                    ptx::umma_commit(empty_bar(stage));
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                ptx::umma_commit(acc_full);
+                acc_phase ^= 1u;
+            }
+        mma_done:;
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+        // ------------------------------------------------------------------- epilogue
+        const int q = warp - kEpiWarp0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            const Problem& pr = p.probs[ti.prob];
+            int ok = 0;
+            if (lane == 0) ok = ptx::mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.err, kSiteAccFull);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !ti.half1) break;
+                const int row = ti.m0 + h * 128 + q * 32 + lane;
+                for (int c = 0; c < pr.bn; c += 32) {
+                    float v[32];
+                    ptx::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * pr.bn + c), v);
+                    if (row < pr.m) epilogue_store(pr, ti.split, row, ti.n0 + c, v);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(acc_empty);
+            acc_phase ^= 1u;
+        }
+    } else if (warp >= kDequantWarp0) {
+        // --------------------------------------------------------------- B producer
+        const int dt = threadIdx.x - kDequantWarp0 * 32;   // 0 .. 255
+        uint32_t stage = 0, phase = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            const Problem& pr = p.probs[ti.prob];
+            for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
+                int ok = 0;
+                if (lane == 0)
+                    ok = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) goto deq_done;
+                {
+                    int si, kk;
+                    locate(p, pr, ks, si, kk);
+                    const KSeg& sg = p.segs[si];
+                    const uint32_t b_dst = sB + stage * kStageBBytes;
+                    if (sg.b_src == B_NF4_K) {
+                        if (dt < pr.bn) {
+                            const Nf4Dev& w = p.nf4[sg.b_idx];
+                            const int64_t wrow = (int64_t)sg.b_n0 + ti.n0 + dt;
+                            const int64_t col0 = (int64_t)sg.b_k0 + (int64_t)kk * kBK;
+                            const uint32_t dst = b_dst + dt * 128;
+                            if (wrow < w.n_out && col0 < w.k_in) {
+                                uint32_t o[32];
+                                nf4_decode_block(w, wrow, col0, lv, o);
+                                smem_row_store(dst, dt & 7, o);
+                            } else {
+                                smem_row_zero(dst);
+                            }
+                        }
+                    } else if (sg.b_src == B_NF4_MN) {
+                        const int j = dt & 63;
+                        const int a = dt >> 6;
+                        if (a < pr.bn / 64) {
+                            const Nf4Dev& w = p.nf4[sg.b_idx];
+                            const int kin = kk * kBK + j;
+                            const int64_t wrow = (int64_t)sg.b_k0 + kin;
+                            const int64_t col0 = (int64_t)sg.b_n0 + ti.n0 + 64 * a;
+                            const uint32_t dst = b_dst + a * 8192 + j * 128;
+                            if (kin < sg.k_len && wrow < w.n_out && col0 < w.k_in) {
+                                uint32_t o[32];
+                                nf4_decode_block(w, wrow, col0, lv, o);
+                                smem_row_store(dst, j & 7, o);
+                            } else {
+                                smem_row_zero(dst);
+                            }
+                        }
+                    } else if (sg.b_src == B_SCALED_K) {
+                        if (dt < pr.bn) {
+                            const int64_t n = (int64_t)ti.n0 + dt;
+                            const uint32_t dst = b_dst + dt * 128;
+                            if (n < sg.b_rows)
+                                smem_row_scaled(dst, dt & 7, sg.b_ptr + n * sg.b_ld, sg.k_len, sg.b_scale);
+                            else
+                                smem_row_zero(dst);
+                        }
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(full_bar(stage));
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+    deq_done:;
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // let copies and MMAs already in flight land before the CTA releases its resources
+        if (threadIdx.x == 0) ptx::settle_ns(50000);
+        __syncthreads();
+    }
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ----------------------------------------------------------------------- split reduce
+
+__global__ void gemm_reduce_kernel(const float* __restrict__ partial, int splits, int m, int n,
+                                   int64_t part_stride, int epi, void* out, int64_t ldo, float alpha,
+                                   const uint16_t* __restrict__ residual, int64_t ldr, int n_valid) {
+    const int n4 = n_valid / 4;
+    const int64_t total = (int64_t)m * n4;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int row, c4;
+        if (epi == EPI_F32_T) {   // consecutive threads on consecutive rows: coalesced stores
+            c4 = (int)(idx / m);
+            row = (int)(idx - (int64_t)c4 * m);
+        } else {
+            row = (int)(idx / n4);
+            c4 = (int)(idx - (int64_t)row * n4);
+        }
+        const int col = c4 * 4;
+        const float* src = partial + (int64_t)row * n + col;
+        float4 acc = *reinterpret_cast<const float4*>(src);
+        for (int s = 1; s < splits; ++s) {
+            const float4 y = *reinterpret_cast<const float4*>(src + (int64_t)s * part_stride);
+            acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+        }
+        float f[4] = {acc.x * alpha, acc.y * alpha, acc.z * alpha, acc.w * alpha};
+        if (epi == EPI_BF16) {
+            if (residual) {
+                const uint2 r2 = *reinterpret_cast<const uint2*>(residual + (int64_t)row * ldr + col);
+                f[0] += __uint_as_float(r2.x << 16);
+                f[1] += __uint_as_float(r2.x & 0xFFFF0000u);
+                f[2] += __uint_as_float(r2.y << 16);
+                f[3] += __uint_as_float(r2.y & 0xFFFF0000u);
+            }
+            uint2 w;
+            w.x = pack_bf16x2(f[0], f[1]);
+            w.y = pack_bf16x2(f[2], f[3]);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + (int64_t)row * ldo + col) = w;
+        } else if (epi == EPI_F32_T) {
+            float* o = static_cast<float*>(out);
+            for (int j = 0; j < 4; ++j) o[(int64_t)(col + j) * ldo + row] = f[j];
+        } else {
+            float* o = static_cast<float*>(out) + (int64_t)row * ldo + col;
+            float4 x = make_float4(f[0], f[1], f[2], f[3]);
+            if (epi == EPI_F32_ACC) {
+                const float4 y = *reinterpret_cast<const float4*>(o);
+                x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+            }
+            *reinterpret_cast<float4*>(o) = x;
+        }
+    }
+}
+
+// --------------------------------------------------------------------- dequant (tests)
+
+__global__ void nf4_dequant_kernel(Nf4Dev w, Nf4Levels lvl, uint16_t* __restrict__ out) {
+    __shared__ float lv[16];
+    if (threadIdx.x < 16) lv[threadIdx.x] = lvl.v[threadIdx.x];
+    __syncthreads();
+    const int64_t nb = w.n_out * (w.k_in / 64);
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nb;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = b / (w.k_in / 64);
+        const int64_t col0 = (b - row * (w.k_in / 64)) * 64;
+        uint32_t o[32];
+        nf4_decode_block(w, row, col0, lv, o);
+        uint4* dst = reinterpret_cast<uint4*>(out + row * w.k_in + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+}
+
+// =========================================================================== host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+int num_sms() {
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+int choose_splits(int64_t tiles, int ksteps) {
+    const int64_t kPlanSMs = 148;
+    if (tiles >= kPlanSMs || ksteps <= 1) return 1;
+    int64_t s = (kPlanSMs + tiles - 1) / tiles;
+    if (s > ksteps) s = ksteps;
+    if (s > 32) s = 32;
+    return (int)s;
+}
+
+GemmPlan::GemmPlan(bool dry) : dry_(dry) { memset(&p_, 0, sizeof(p_)); }
+
+int GemmPlan::map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    if (status_) return -1;
+    if (n_maps_ >= kMaxMaps) return status_ = fail(LSN_EINVAL, "gemm: too many tensor maps");
+    map_box_[n_maps_] = box_rows;
+    if (dry_) return n_maps_++;
+    if (!ptr || rows < 1 || cols < 1 || ld < cols || (reinterpret_cast<uintptr_t>(ptr) & 15) ||
+        (ld * 2) % 16 || box_rows < 1 || box_rows > 256)
+        return status_ = fail(LSN_EINVAL, "gemm: operand must be 16-byte aligned with 16-byte rows");
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return status_ = fail(LSN_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(&p_.maps[n_maps_], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return status_ = fail(LSN_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return n_maps_++;
+}
+
+int GemmPlan::nf4(const void* base, int64_t n_out, int64_t k_in) {
+    if (status_) return -1;
+    Nf4Layout L;
+    if (n_nf4_ >= kMaxNf4) return status_ = fail(LSN_EINVAL, "gemm: too many NF4 matrices");
+    if (dry_) {
+        p_.nf4[n_nf4_].n_out = n_out;
+        p_.nf4[n_nf4_].k_in = k_in;
+        return n_nf4_++;
+    }
+    if (!base || (reinterpret_cast<uintptr_t>(base) & 15) || !nf4_layout(n_out, k_in, &L))
+        return status_ = fail(LSN_EINVAL, "gemm: bad NF4 view");
+    const uint8_t* b = static_cast<const uint8_t*>(base);
+    Nf4Dev& d = p_.nf4[n_nf4_];
+    d.codes = b + L.codes;
+    d.absmax = b + L.absmax;
+    d.scale = reinterpret_cast<const float*>(b + L.scale);
+    d.offset = reinterpret_cast<const float*>(b + L.offset);
+    d.n_out = n_out;
+    d.k_in = k_in;
+    return n_nf4_++;
+}
+
+int GemmPlan::problem(int m, int n, int bn, int a_major, int epi, void* out, int64_t ldo, float alpha,
+                      int n_valid, int splits, const uint16_t* residual, int64_t ldr) {
+    if (status_) return -1;
+    if (p_.n_probs >= kMaxProbs) return status_ = fail(LSN_EINVAL, "gemm: too many problems");
+    if (m < 1 || n < 1 || !(bn == 64 || bn == 128 || bn == 256) || (!out && !dry_) || n_valid < 1 ||
+        n_valid > n || n_valid % 8 || splits < 1 || (reinterpret_cast<uintptr_t>(out) & 15))
+        return status_ = fail(LSN_EINVAL, "gemm: bad problem");
+    Problem& pr = p_.probs[p_.n_probs];
+    memset(&pr, 0, sizeof(pr));
+    pr.m = m;
+    pr.n = n;
+    pr.bn = bn;
+    pr.a_major = a_major;
+    pr.seg_begin = n_segs_;
+    pr.seg_count = 0;
+    pr.splits = splits;
+    pr.epi = epi;
+    pr.out = out;
+    pr.ldo = ldo;
+    pr.alpha = alpha;
+    pr.n_valid = n_valid;
+    pr.residual = residual;
+    pr.ldr = ldr;
+    return p_.n_probs++;
+}
+
+int GemmPlan::seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len) {
+    if (status_) return -1;
+    if (p_.n_probs == 0 || n_segs_ >= kMaxSegs || k_len < 1 || (a_k0 % 8) || a_map < 0 || a_map >= n_maps_)
+        return status_ = fail(LSN_EINVAL, "gemm: bad segment");
+    if ((b_src == B_TMA_K || b_src == B_TMA_MN) && (b_idx < 0 || b_idx >= n_maps_))
+        return status_ = fail(LSN_EINVAL, "gemm: bad B map");
+    {
+        // every TMA box must deliver exactly the bytes the kernel expects for its stage
+        const Problem& pr = p_.probs[p_.n_probs - 1];
+        const int want_a = pr.a_major == A_KMAJOR ? kBM : 64;
+        if (map_box_[a_map] != want_a) return status_ = fail(LSN_EINVAL, "gemm: A map box rows mismatch");
+        if (b_src == B_TMA_K && map_box_[b_idx] != pr.bn)
+            return status_ = fail(LSN_EINVAL, "gemm: K-major B map box rows must equal the N tile");
+        if (b_src == B_TMA_MN && map_box_[b_idx] != 64)
+            return status_ = fail(LSN_EINVAL, "gemm: MN-major B map box rows must be 64");
+    }
+    if ((b_src == B_NF4_K || b_src == B_NF4_MN) && (b_idx < 0 || b_idx >= n_nf4_ || b_k0 % 64 || b_n0 % 64))
+        return status_ = fail(LSN_EINVAL, "gemm: bad NF4 segment");
+    KSeg& s = p_.segs[n_segs_];
+    memset(&s, 0, sizeof(s));
+    s.a_map = a_map;
+    s.a_k0 = a_k0;
+    s.b_src = b_src;
+    s.b_idx = b_idx;
+    s.b_k0 = b_k0;
+    s.b_n0 = b_n0;
+    s.k_len = k_len;
+    s.ksteps = (k_len + kBK - 1) / kBK;
+    Problem& pr = p_.probs[p_.n_probs - 1];
+    pr.seg_count++;
+    pr.ksteps += s.ksteps;
+    return n_segs_++;
+}
+
+int GemmPlan::seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, int b_rows, int k_len,
+                         float b_scale) {
+    if (status_) return -1;
+    if ((!b_ptr && !dry_) || k_len < 8 || k_len > 64 || k_len % 8 || b_ld % 8 ||
+        (reinterpret_cast<uintptr_t>(b_ptr) & 15))
+        return status_ = fail(LSN_EINVAL, "gemm: bad scaled segment");
+    int s = seg(a_map, a_k0, B_SCALED_K, 0, 0, 0, k_len);
+    if (s < 0) return s;
+    p_.segs[s].b_ptr = b_ptr;
+    p_.segs[s].b_ld = b_ld;
+    p_.segs[s].b_rows = b_rows;
+    p_.segs[s].b_scale = b_scale;
+    return s;
+}
+
+size_t GemmPlan::partial_bytes() const {
+    size_t b = 0;
+    for (int i = 0; i < p_.n_probs; ++i) {
+        const Problem& pr = p_.probs[i];
+        const int splits = pr.splits > pr.ksteps ? pr.ksteps : pr.splits;
+        if (splits > 1) b += (size_t)splits * pr.m * pr.n * sizeof(float);
+    }
+    return b;
+}
+
+int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
+    if (status_) return status_;
+    if (p_.n_probs == 0) return LSN_OK;
+    if (dry_) return LSN_OK;
+    // partial-sum slabs for split problems
+    struct Final { int epi; void* out; int64_t ldo; float alpha; const uint16_t* res; int64_t ldr; };
+    Final fin[kMaxProbs];
+    size_t off = 0;
+    int tiles = 0;
+    for (int i = 0; i < p_.n_probs; ++i) {
+        Problem& pr = p_.probs[i];
+        if (pr.seg_count == 0) return status_ = fail(LSN_EINVAL, "gemm: problem without segments");
+        if (pr.splits > pr.ksteps) pr.splits = pr.ksteps;
+        pr.tiles_m = (pr.m + kBM - 1) / kBM;
+        pr.tiles_n = (pr.n + pr.bn - 1) / pr.bn;
+        pr.tile_begin = tiles;
+        tiles += pr.tiles_m * pr.tiles_n * pr.splits;
+        fin[i] = {pr.epi, pr.out, pr.ldo, pr.alpha, pr.residual, pr.ldr};
+        if (pr.splits > 1) {
+            const size_t need = (size_t)pr.splits * pr.m * pr.n * sizeof(float);
+            if (!partial_ws || off + need > ws_bytes)
+                return status_ = fail(LSN_ENOMEM, "gemm: split-K workspace too small");
+            pr.out = reinterpret_cast<uint8_t*>(partial_ws) + off;
+            pr.ldo = pr.n;
+            pr.part_stride = (int64_t)pr.m * pr.n;
+            pr.epi = EPI_PARTIAL;
+            pr.residual = nullptr;
+            off += need;
+        }
+    }
+    p_.total_tiles = tiles;
+    memcpy(p_.levels, nf4_levels(), sizeof(p_.levels));
+    p_.err = device_error_word();
+    if (!p_.err) return LSN_ECUDA;
+
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        LSN_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kGemmSmemBytes));
+        attr_set[dev] = true;
+    }
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    tc_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(p_);
+    LSN_CUDA_TRY(cudaGetLastError());
+    for (int i = 0; i < p_.n_probs; ++i) {
+        const Problem& pr = p_.probs[i];
+        if (pr.epi != EPI_PARTIAL) continue;
+        int rc = gemm_reduce(static_cast<const float*>(pr.out), pr.splits, pr.m, pr.n, pr.part_stride,
+                             fin[i].epi, fin[i].out, fin[i].ldo, fin[i].alpha, fin[i].res, fin[i].ldr,
+                             pr.n_valid, s);
+        if (rc) return rc;
+    }
+    return LSN_OK;
+}
+
+int gemm_reduce(const float* partial, int splits, int m, int n, int64_t part_stride, int epi, void* out,
+                int64_t ldo, float alpha, const uint16_t* residual, int64_t ldr, int n_valid,
+                cudaStream_t s) {
+    const int64_t total = (int64_t)m * (n_valid / 4);
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    gemm_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(partial, splits, m, n, part_stride, epi, out, ldo,
+                                                        alpha, residual, ldr, n_valid);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+int nf4_dequant_launch(const Nf4Dev& w, uint16_t* out, cudaStream_t s) {
+    Nf4Levels l;
+    memcpy(l.v, nf4_levels(), sizeof(l.v));
+    const int64_t nb = w.n_out * (w.k_in / 64);
+    int64_t blocks = (nb + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    nf4_dequant_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, l, out);
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+}  // namespace lsn

@@ -1,0 +1,149 @@
+// Grouped tcgen05 GEMM with an NF4-dequantising operand producer (internal interface).
+//
+// One launch runs up to kMaxProbs independent GEMM "problems"
+//     D[m x n] = sum over K-segments of  A_seg[m x k] * B_seg[n x k]^T
+// on a persistent grid.  A always arrives by TMA (K-major or MN-major tiles).  B arrives by
+// TMA (dense bf16), is decoded from packed NF4 by producer warps straight into the
+// swizzled shared-memory operand layout (K-major for y = x W^T, MN-major for dX = dY W), or
+// is loaded and scaled by the producer warps (the LoRA B factor times s).  Accumulation is
+// fp32 in TMEM; the epilogue writes bf16, fp32, fp32 added into the output, fp32 transposed,
+// or fp32 split-K partials that gemm_reduce sums in a fixed order.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lsn {
+
+constexpr int kBM = 256;        // rows per tile: two M=128 UMMA halves share each B tile
+constexpr int kBK = 64;         // contraction per stage: one NF4 block, one 128-byte row
+constexpr int kStages = 3;
+constexpr int kMaxBN = 256;
+constexpr int kStageABytes = kBM * kBK * 2;
+constexpr int kStageBBytes = kMaxBN * kBK * 2;
+constexpr int kGemmThreads = 512;
+constexpr int kMaxMaps = 16;
+constexpr int kMaxNf4 = 8;
+constexpr int kMaxSegs = 20;
+constexpr int kMaxProbs = 16;
+
+enum ASrc : int { A_KMAJOR = 0, A_MNMAJOR = 1 };
+enum BSrc : int {
+    B_NF4_K = 0,     // packed NF4 W [n_out x k_in]; tile rows = W rows (output n)
+    B_NF4_MN = 1,    // packed NF4 W; contraction over W rows, output over W columns
+    B_TMA_K = 2,     // dense bf16 [n x k] via TMA, K-major
+    B_TMA_MN = 3,    // dense bf16 [k x n] via TMA, MN-major
+    B_SCALED_K = 4,  // dense bf16 [n x k<=64] loaded and multiplied by b_scale
+};
+enum Epi : int {
+    EPI_BF16 = 0,     // out bf16 = alpha*acc (+ residual)
+    EPI_F32 = 1,      // out fp32 = alpha*acc
+    EPI_F32_ACC = 2,  // out fp32 += alpha*acc
+    EPI_F32_T = 3,    // out fp32 [n x m] (transposed) = alpha*acc
+    EPI_PARTIAL = 4,  // partial fp32 [split][m][n] = acc (reduced by gemm_reduce)
+};
+
+struct KSeg {
+    int a_map;         // tensor map of A
+    int a_k0;          // contraction offset into A (elements)
+    int b_src;
+    int b_idx;         // NF4 view index (B_NF4_*) or tensor map (B_TMA_*)
+    int b_k0;          // contraction offset into B
+    int b_n0;          // output offset into B
+    int k_len;         // contraction length of the segment
+    int ksteps;        // ceil(k_len / 64)
+    const uint16_t* b_ptr;  // B_SCALED_K: rows of length b_ld
+    int b_ld;
+    int b_rows;        // B_SCALED_K: valid rows
+    float b_scale;
+};
+
+struct Problem {
+    int m, n;          // output rows / columns
+    int bn;            // N tile: 64, 128 or 256
+    int a_major;
+    int seg_begin, seg_count;
+    int ksteps;        // total over the segments
+    int splits;
+    int tiles_m, tiles_n;
+    int tile_begin;
+    int epi;
+    void* out;
+    int64_t ldo;       // output leading dimension (elements); for EPI_F32_T: row stride of out
+    const uint16_t* residual;
+    int64_t ldr;
+    float alpha;
+    int n_valid;       // columns to write
+    int64_t part_stride;  // EPI_PARTIAL: elements per split slab (m * n)
+};
+
+struct Nf4Dev {
+    const uint8_t* codes;
+    const uint8_t* absmax;
+    const float* scale;
+    const float* offset;
+    int64_t n_out, k_in;
+};
+
+struct GemmParams {   // 128-byte aligned through CUtensorMap
+    CUtensorMap maps[kMaxMaps];
+    Nf4Dev nf4[kMaxNf4];
+    KSeg segs[kMaxSegs];
+    Problem probs[kMaxProbs];
+    float levels[16];
+    uint32_t* err;
+    int n_probs;
+    int total_tiles;
+};
+
+// Host-side assembly of one grouped launch.
+class GemmPlan {
+   public:
+    // dry: shapes only (no pointers are checked, no tensor maps encoded, nothing launched);
+    // used to size workspaces with exactly the split decisions of the real launch.
+    explicit GemmPlan(bool dry = false);
+    // Dense bf16 matrix [rows x cols] (row stride ld elements) as an A or B operand.
+    // kmajor: box 64 (cols) x box_rows; otherwise box 64 x 64.  Returns the map index or < 0.
+    int map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows);
+    int nf4(const void* base, int64_t n_out, int64_t k_in);
+    // Starts a problem; segments added next belong to it.
+    int problem(int m, int n, int bn, int a_major, int epi, void* out, int64_t ldo, float alpha,
+                int n_valid, int splits = 1, const uint16_t* residual = nullptr,
+                int64_t ldr = 0);
+    int seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len);
+    int seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, int b_rows, int k_len,
+                   float b_scale);
+    // Bytes of split-K partial workspace the launch needs (after clamping splits).
+    size_t partial_bytes() const;
+    // Launches the GEMM and the split reductions (a dry plan only validates).
+    int launch(cudaStream_t s, float* partial_ws, size_t ws_bytes);
+    int status() const { return status_; }
+
+   private:
+    GemmParams p_;
+    int n_maps_ = 0, n_nf4_ = 0, n_segs_ = 0;
+    int map_box_[kMaxMaps] = {0};   // box rows of each map (the kernel's byte counts rely on it)
+    int status_ = 0;
+    bool dry_ = false;
+};
+
+// Sums the split partials of EPI_PARTIAL problems in split order and applies the final
+// epilogue (bf16 / f32 / f32 += / transposed f32, alpha, residual).
+int gemm_reduce(const float* partial, int splits, int m, int n, int64_t part_stride, int epi,
+                void* out, int64_t ldo, float alpha, const uint16_t* residual, int64_t ldr,
+                int n_valid, cudaStream_t s);
+
+int num_sms();
+
+// Split count for a problem of `tiles` output tiles and `ksteps` contraction steps, chosen
+// for a fixed 148-SM machine so that the summation order never depends on the device.
+int choose_splits(int64_t tiles, int ksteps);
+
+struct Nf4Levels {
+    float v[16];
+};
+// Test-only decode of a whole packed matrix to bf16 in HBM (same decode as the GEMM).
+int nf4_dequant_launch(const Nf4Dev& w, uint16_t* out, cudaStream_t s);
+
+}  // namespace lsn

@@ -1,0 +1,162 @@
+"""GPU parity of the single NF4 linear + LoRA (through the C ABI) against the fp64 oracle.
+
+Bars: dequantised weights bit-exact; forward max|y - y_ref| / max|y_ref| <= 2e-2; gradients
+||g - g_ref||_F / ||g_ref||_F <= 1e-2; repeated launches bit-identical."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FWD_TOL = 2e-2
+GRAD_TOL = 1e-2
+
+
+def _lsn():
+    import layer_streamed_nf4_quant_b300 as lsn
+    return lsn
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _bits(t):
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _f64_of_bits(bits):
+    from oracle.nf4 import bf16_value
+    return bf16_value(bits).astype(np.float64)
+
+
+def _max_rel(got, ref):
+    return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+
+
+def _fro_rel(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def _case(M, N, K, r, seed):
+    from synth import random_bf16
+    rng = np.random.default_rng(seed)
+    W = (0.02 * rng.standard_normal((N, K))).astype(np.float32)
+    X = random_bf16((M, K), seed + 1)
+    A = random_bf16((r, K), seed + 2, std=1.0 / np.sqrt(K))
+    B = random_bf16((N, r), seed + 3, std=0.01)
+    dY = random_bf16((M, N), seed + 4)
+    return {"X": X, "W": W, "A": A, "B": B, "dY": dY}
+
+
+def _run_and_compare(inp, r, scale, residual=False):
+    from oracle import lora as olora
+    from oracle import nf4 as onf4
+    lsn = _lsn()
+    W = inp["W"]
+    N, K = W.shape
+    M = inp["X"].shape[0]
+    packed = torch.from_numpy(lsn.nf4_pack(W)).cuda()
+    X, A, B, dY = (_bf16_dev(inp[k]) for k in ("X", "A", "B", "dY"))
+    res = _bf16_dev(inp["R"]) if residual else None
+    Y, T = lsn.lora_nf4_fwd(packed, N, K, X, A, B, r, scale, residual=res)
+    dX, dA, dB = lsn.lora_nf4_bwd(packed, N, K, X, T, dY, A, B, r, scale)
+    torch.cuda.synchronize()
+    assert lsn.device_check() == 0
+
+    Wh = onf4.dequantize(onf4.quantize(W))
+    Xf, Af, Bf, dYf = (_f64_of_bits(inp[k]) for k in ("X", "A", "B", "dY"))
+    Yr, Tr = olora.lora_forward(Xf, Wh, Af, Bf, scale)
+    if residual:
+        Yr = Yr + _f64_of_bits(inp["R"])
+    dXr, dAr, dBr = olora.lora_backward(Xf, Wh, Af, Bf, Tr, dYf, scale)
+    out = {
+        "Y": _max_rel(_f64_of_bits(_bits(Y)), Yr),
+        "T": _max_rel(_f64_of_bits(_bits(T)), Tr),
+        "dX": _fro_rel(dX.double().cpu().numpy(), dXr),
+        "dA": _fro_rel(dA.double().cpu().numpy(), dAr),
+        "dB": _fro_rel(dB.double().cpu().numpy(), dBr),
+    }
+    return out, (Y, T, dX, dA, dB)
+
+
+def test_dequant_bit_exact_workload_weights():
+    from oracle import nf4 as onf4
+    from synth import single_linear_inputs
+    lsn = _lsn()
+    W = single_linear_inputs()["W"]
+    packed = torch.from_numpy(lsn.nf4_pack(W)).cuda()
+    got = _bits(lsn.nf4_dequant(packed, *W.shape))
+    np.testing.assert_array_equal(got, onf4.dequantize_bf16_bits(onf4.quantize(W)))
+
+
+def test_gemm_identity_input_gives_dequantised_weights_exactly():
+    """X = I, B = 0: each output is one exact product plus exact zeros, so the GEMM's
+    on-chip decode must reproduce the oracle's dequantised weights bit for bit."""
+    from oracle import nf4 as onf4
+    from synth import f32_to_bf16_bits, single_linear_inputs
+    lsn = _lsn()
+    W = single_linear_inputs()["W"]                      # [1024 x 512]
+    N, K = W.shape
+    packed = torch.from_numpy(lsn.nf4_pack(W)).cuda()
+    X = _bf16_dev(f32_to_bf16_bits(np.eye(K, dtype=np.float32)))
+    A = _bf16_dev(f32_to_bf16_bits(np.full((8, K), 0.25, np.float32)))
+    B = torch.zeros((N, 8), dtype=torch.bfloat16, device="cuda")
+    Y, _ = lsn.lora_nf4_fwd(packed, N, K, X, A, B, 8, 2.0)
+    torch.cuda.synchronize()
+    want = onf4.dequantize_bf16_bits(onf4.quantize(W)).T
+    np.testing.assert_array_equal(_bits(Y), want)
+
+
+def test_single_linear_workload_parity():
+    """The single-linear workload: X [128x512], W [1024x512], r = 8, alpha = 16."""
+    from synth import single_linear_inputs
+    inp = single_linear_inputs()
+    err, _ = _run_and_compare(inp, 8, 16.0 / 8)
+    assert err["Y"] <= FWD_TOL and err["T"] <= FWD_TOL, err
+    for k in ("dX", "dA", "dB"):
+        assert err[k] <= GRAD_TOL, err
+
+
+@pytest.mark.parametrize("M,N,K,r", [(1, 64, 64, 8), (100, 320, 192, 16), (300, 512, 256, 64),
+                                     (513, 1024, 512, 24), (257, 776, 1088, 64)])
+def test_ragged_shapes_parity(M, N, K, r):
+    inp = _case(M, N, K, r, seed=M + N + K + r)
+    err, _ = _run_and_compare(inp, r, 16.0 / r)
+    assert err["Y"] <= FWD_TOL and err["T"] <= FWD_TOL, err
+    for k in ("dX", "dA", "dB"):
+        assert err[k] <= GRAD_TOL, err
+
+
+def test_residual_epilogue():
+    from synth import random_bf16
+    inp = _case(200, 256, 128, 8, seed=5)
+    inp["R"] = random_bf16((200, 256), 99)
+    err, _ = _run_and_compare(inp, 8, 2.0, residual=True)
+    assert err["Y"] <= FWD_TOL, err
+
+
+def test_repeated_launches_bit_identical():
+    from synth import single_linear_inputs
+    inp = single_linear_inputs()
+    _, a = _run_and_compare(inp, 8, 2.0)
+    _, b = _run_and_compare(inp, 8, 2.0)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
+def test_accumulate_dx_and_zero_A_gives_zero_dB():
+    lsn = _lsn()
+    inp = _case(64, 128, 128, 8, seed=11)
+    N, K = inp["W"].shape
+    packed = torch.from_numpy(lsn.nf4_pack(inp["W"])).cuda()
+    X, B, dY = (_bf16_dev(inp[k]) for k in ("X", "B", "dY"))
+    A0 = torch.zeros((8, K), dtype=torch.bfloat16, device="cuda")
+    Y, T = lsn.lora_nf4_fwd(packed, N, K, X, A0, B, 8, 2.0)
+    dX1, dA, dB = lsn.lora_nf4_bwd(packed, N, K, X, T, dY, A0, B, 8, 2.0)
+    assert torch.count_nonzero(T) == 0 and torch.count_nonzero(dB) == 0
+    dX2 = dX1.clone()
+    lsn.lora_nf4_bwd(packed, N, K, X, T, dY, A0, B, 8, 2.0, dX=dX2, accumulate_dX=True)
+    torch.cuda.synchronize()
+    assert torch.allclose(dX2, 2 * dX1, rtol=1e-6, atol=1e-6)
