@@ -54,6 +54,21 @@ int lsn_abi_version(void);
  * synchronisation itself failed.  `detail` (nullable, host) receives the raw word. */
 int lsn_check(void* stream, uint32_t* detail);
 
+/* Launch accounting and opt-in kernel timing (process-wide).
+ * lsn_launch_count: number of kernels this library has launched so far (all devices).
+ * lsn_profile_enable(1): from then on every GEMM launch is bracketed by two CUDA events on
+ * its own stream and its algorithmic FLOPs (2 * m * n * k summed over its problems, no
+ * padding) are recorded; lsn_profile_read synchronises on those events, adds their device
+ * times up and (reset != 0) clears the totals. */
+typedef struct {
+    uint64_t gemm_launches;   /* timed GEMM launches since the last reset */
+    double   gemm_ms;         /* summed device time of those launches     */
+    double   gemm_flops;      /* summed algorithmic FLOPs of those launches */
+} lsn_profile;
+uint64_t lsn_launch_count(void);
+int lsn_profile_enable(int on);
+int lsn_profile_read(lsn_profile* out, int reset);
+
 /* ------------------------------------------------------------------------------ NF4 ---
  * NF4 storage of the frozen base ([P1] "Why NF4 matters so much": QLoRA's 4-bit NormalFloat,
  * about a quarter of bf16).  Codebook: the 16 QLoRA levels -- standard-normal quantiles at

@@ -13,7 +13,7 @@ import ctypes as C
 import numpy as np
 
 from ._lib import (LSN_ECORRUPT, LSN_EINVAL, LSN_ENOMEM, LSN_ESTATE, LSN_ETIMEOUT, LSN_OK,  # noqa: F401
-                   LsnError, check, lib, lsn_pool_stats, lsn_stack_desc, nf4_view)
+                   LsnError, check, lib, lsn_pool_stats, lsn_profile, lsn_stack_desc, nf4_view)
 
 PROJ = ("q", "k", "v", "gate", "up", "o", "down")   # canonical projection order
 
@@ -121,6 +121,22 @@ def device_check(stream=None) -> int:
     detail = C.c_uint32(0)
     check(lib.lsn_check(_stream(stream), C.byref(detail)))
     return detail.value
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib.lsn_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    check(lib.lsn_profile_enable(1 if on else 0))
+
+
+def profile_read(reset: bool = False) -> dict:
+    """GEMM launches timed with CUDA events since the last reset: count, ms, FLOPs."""
+    p = lsn_profile()
+    check(lib.lsn_profile_read(C.byref(p), 1 if reset else 0))
+    return {"gemm_launches": p.gemm_launches, "gemm_ms": p.gemm_ms, "gemm_flops": p.gemm_flops}
 
 
 # ------------------------------------------------------------------------ stream pool

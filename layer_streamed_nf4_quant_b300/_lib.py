@@ -40,6 +40,10 @@ class lsn_stack_desc(C.Structure):
                 ("rms_eps", C.c_float), ("kv_loss_coef", C.c_float)]
 
 
+class lsn_profile(C.Structure):
+    _fields_ = [("gemm_launches", C.c_uint64), ("gemm_ms", C.c_double), ("gemm_flops", C.c_double)]
+
+
 P = C.c_void_p
 I = C.c_int
 I64 = C.c_int64
@@ -51,6 +55,9 @@ SIGNATURES = {
     "lsn_last_error": (C.c_char_p, []),
     "lsn_abi_version": (I, []),
     "lsn_check": (I, [P, C.POINTER(C.c_uint32)]),
+    "lsn_launch_count": (C.c_uint64, []),
+    "lsn_profile_enable": (I, [I]),
+    "lsn_profile_read": (I, [C.POINTER(lsn_profile), I]),
     "lsn_nf4_codebook": (I, [C.POINTER(F)]),
     "nf4_packed_bytes": (SZ, [I64, I64]),
     "nf4_pack": (I, [P, I64, I64, P, SZ, I]),

@@ -62,6 +62,54 @@ uint32_t* device_error_word() {
     return g_dev_err[dev];
 }
 
+// ------------------------------------------------------------------- launch accounting
+
+static std::atomic<uint64_t> g_launches(0);
+static std::atomic<bool> g_profiling(false);
+
+struct ProfEvent {
+    cudaEvent_t start, end;
+    double flops;
+};
+static std::mutex g_prof_mu;
+static std::vector<ProfEvent> g_prof_pending, g_prof_spare;
+static uint64_t g_prof_launches = 0;
+static double g_prof_ms = 0.0, g_prof_flops = 0.0;
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+bool profiling() { return g_profiling.load(std::memory_order_relaxed); }
+
+void* profile_begin(cudaStream_t s) {
+    if (!profiling()) return nullptr;
+    ProfEvent* e = new (std::nothrow) ProfEvent();
+    if (!e) return nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        if (!g_prof_spare.empty()) {
+            *e = g_prof_spare.back();
+            g_prof_spare.pop_back();
+        } else if (cudaEventCreate(&e->start) != cudaSuccess || cudaEventCreate(&e->end) != cudaSuccess) {
+            delete e;
+            return nullptr;
+        }
+    }
+    if (cudaEventRecord(e->start, s) != cudaSuccess) {
+        delete e;
+        return nullptr;
+    }
+    return e;
+}
+
+void profile_end(void* token, cudaStream_t s, double flops) {
+    if (!token) return;
+    ProfEvent* e = static_cast<ProfEvent*>(token);
+    e->flops = flops;
+    cudaEventRecord(e->end, s);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_pending.push_back(*e);
+    delete e;
+}
+
 // ------------------------------------------------------------------------- codebook
 // Standard-normal upper quantile by Newton's method on the complementary error function:
 // solve 0.5*erfc(x/sqrt(2)) = 1 - p for x, starting from the Abramowitz-Stegun 26.2.23
@@ -291,6 +339,40 @@ extern "C" {
 const char* lsn_last_error(void) { return g_err; }
 
 int lsn_abi_version(void) { return 1; }
+
+uint64_t lsn_launch_count(void) { return g_launches.load(); }
+
+int lsn_profile_enable(int on) {
+    g_profiling.store(on != 0);
+    return LSN_OK;
+}
+
+int lsn_profile_read(lsn_profile* out, int reset) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& e : g_prof_pending) {
+        cudaError_t r = cudaEventSynchronize(e.end);
+        if (r != cudaSuccess) return cuda_fail(r, "lsn_profile_read: cudaEventSynchronize");
+        float ms = 0.f;
+        r = cudaEventElapsedTime(&ms, e.start, e.end);
+        if (r != cudaSuccess) return cuda_fail(r, "lsn_profile_read: cudaEventElapsedTime");
+        g_prof_ms += ms;
+        g_prof_flops += e.flops;
+        g_prof_launches += 1;
+        g_prof_spare.push_back(e);
+    }
+    g_prof_pending.clear();
+    if (out) {
+        out->gemm_launches = g_prof_launches;
+        out->gemm_ms = g_prof_ms;
+        out->gemm_flops = g_prof_flops;
+    }
+    if (reset) {
+        g_prof_launches = 0;
+        g_prof_ms = 0.0;
+        g_prof_flops = 0.0;
+    }
+    return LSN_OK;
+}
 
 int lsn_check(void* stream, uint32_t* detail) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

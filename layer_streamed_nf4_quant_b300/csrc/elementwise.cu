@@ -308,6 +308,7 @@ int launch_rmsnorm_fwd(const uint16_t* x, uint16_t* h, float* rstd, int M, int D
     if (header && !err) return LSN_ECUDA;
     rmsnorm_fwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, h, rstd, M, D, eps,
                                                    static_cast<const LayerHeader*>(header), layer, err);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
@@ -316,6 +317,7 @@ int launch_tag_check(const void* header, uint32_t layer, cudaStream_t s) {
     uint32_t* err = device_error_word();
     if (!err) return LSN_ECUDA;
     tag_check_kernel<<<1, 32, 0, s>>>(static_cast<const LayerHeader*>(header), layer, err);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
@@ -323,18 +325,21 @@ int launch_tag_check(const void* header, uint32_t layer, cudaStream_t s) {
 int launch_rmsnorm_bwd(const uint16_t* x, const float* rstd, const float* dh, float* dx, uint16_t* dx_bf,
                        int M, int D, cudaStream_t s) {
     rmsnorm_bwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, rstd, dh, dx, dx_bf, M, D);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
 
 int launch_silu_mul(const uint16_t* y, int64_t ldy, int og, int ou, uint16_t* a, int M, int F, cudaStream_t s) {
     silu_mul_kernel<<<grid_for((int64_t)M * F / 8, 256), 256, 0, s>>>(y, ldy, og, ou, a, M, F);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
 
 int launch_kv_sumsq(const uint16_t* y, int64_t ldy, int ok, int ov, int dkv, int M, float* part, cudaStream_t s) {
     kv_sumsq_kernel<<<kLossBlocks, 256, 0, s>>>(y, ldy, ok, ov, dkv, M, part);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
@@ -343,9 +348,11 @@ int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv
                 float* xpart, const float* kvpart, float* loss, cudaStream_t s) {
     const double md = (double)M * (double)D;
     loss_seed_kernel<<<kLossBlocks, 256, 0, s>>>(x, M, D, (float)(1.0 / md), dx, dx_bf, xpart);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     loss_final_kernel<<<1, 32, 0, s>>>(xpart, kvpart, n_layers, kLossBlocks, 1.0 / md,
                                        (double)kv_coef / ((double)M * (double)dkv), loss);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
@@ -354,6 +361,7 @@ int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, in
                     float kv_coef, cudaStream_t s) {
     const int64_t work = (int64_t)M * (D / 8 + 2 * dkv / 8 + F / 8);
     dy_build_kernel<<<grid_for(work, 256), 256, 0, s>>>(dqa, y, dy, M, D, dkv, F, kv_coef);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }

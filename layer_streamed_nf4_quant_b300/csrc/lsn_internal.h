@@ -28,6 +28,13 @@ enum DeviceErrorKind : uint32_t {
     kDevErrTag = 2u,       // layer image tag mismatch (detail: expected layer)
 };
 
+// Launch accounting: every kernel launch site calls note_launch().
+void note_launch();
+// GEMM profiling hooks (no-ops unless lsn_profile_enable(1) was called).
+bool profiling();
+void* profile_begin(cudaStream_t s);                       // returns a token or nullptr
+void profile_end(void* token, cudaStream_t s, double flops);
+
 // NF4 codebook as computed by the library (host, fp32, ascending).
 const float* nf4_levels();
 

@@ -741,8 +741,20 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
         attr_set[dev] = true;
     }
     const int grid = tiles < num_sms() ? tiles : num_sms();
+    void* prof = profile_begin(s);
     tc_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(p_);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
+    if (prof) {
+        double flops = 0.0;
+        for (int i = 0; i < p_.n_probs; ++i) {
+            const Problem& pr = p_.probs[i];
+            double k = 0.0;
+            for (int j = 0; j < pr.seg_count; ++j) k += (double)p_.segs[pr.seg_begin + j].k_len;
+            flops += 2.0 * (double)pr.m * (double)pr.n_valid * k;
+        }
+        profile_end(prof, s, flops);
+    }
     for (int i = 0; i < p_.n_probs; ++i) {
         const Problem& pr = p_.probs[i];
         if (pr.epi != EPI_PARTIAL) continue;
@@ -764,6 +776,7 @@ int gemm_reduce(const float* partial, int splits, int m, int n, int64_t part_str
     if (blocks < 1) blocks = 1;
     gemm_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(partial, splits, m, n, part_stride, epi, out, ldo,
                                                         alpha, residual, ldr, n_valid);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
@@ -776,6 +789,7 @@ int nf4_dequant_launch(const Nf4Dev& w, uint16_t* out, cudaStream_t s) {
     const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
     nf4_dequant_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, l, out);
+    note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
 }
