@@ -1,6 +1,8 @@
 """Builds the in-tree C-ABI library ``liblsn.so`` with nvcc for sm_103a.
 
-    python -m layer_streamed_nf4_quant_b300.build [--force] [-v]
+    python layer_streamed_nf4_quant_b300/build.py [--force] [-v]
+
+(Run it by path: importing the package loads the library, which may not exist yet.)
 
 Objects go to ``_build/`` at the repository root; the library lands next to this file, where
 the Python binding loads it from.  Only files whose sources (or headers) changed are rebuilt.
