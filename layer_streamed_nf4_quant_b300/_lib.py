@@ -87,7 +87,7 @@ SIGNATURES = {
 def load() -> C.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m layer_streamed_nf4_quant_b300.build`")
+            f"{LIB_PATH} is missing: build it with `python layer_streamed_nf4_quant_b300/build.py`")
     lib = C.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
