@@ -132,6 +132,23 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M,
                  const uint16_t* residual /* nullable */, uint16_t* Y, uint16_t* T_out,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* lora_nf4_fwd for callers that cannot allocate device memory (a plug-in inside a framework
+ * that owns all device memory, or a serving path that must not enter the allocator).  The
+ * pages have no counterpart of it.  Same arguments and results as lora_nf4_fwd, bit for bit,
+ * but no workspace: the split-K partial sums go to a 16 MiB file-scope __device__ buffer and
+ * device-side wait timeouts to a file-scope __device__ word, both held by every GPU that
+ * loads the library until the process exits.  It calls no cudaMalloc/cudaFree (with the
+ * opt-in profiler off).  Its first call on each device looks the buffers' addresses up with
+ * cudaGetSymbolAddress and clears the word (synchronously), so make that first call before
+ * any stream capture.  All calls on a device share the buffer: calls whose kernels overlap on
+ * the GPU race.  A shape whose split-K partials exceed 16 MiB is rejected with LSN_ENOMEM.
+ * device_status (host, nullable): if given, the call synchronises `stream`, stores the word
+ * there, clears it and returns LSN_ETIMEOUT if a device wait ran out. */
+int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X, int64_t M,
+                                const uint16_t* A, const uint16_t* B, int r, float scale,
+                                const uint16_t* residual /* nullable */, uint16_t* Y,
+                                uint16_t* T_out, uint32_t* device_status, void* stream);
+
 /* accumulate_dX != 0 adds into dX instead of overwriting it.  dX may be NULL (skipped). */
 int lora_nf4_bwd(const nf4_view* W, const uint16_t* X, const uint16_t* T, const uint16_t* dY,
                  int64_t M, const uint16_t* A, const uint16_t* B, int r, float scale,

@@ -95,6 +95,25 @@ def lora_nf4_fwd(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, 
     return Y, T
 
 
+def lora_nf4_fwd_static_scratch(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, T=None,
+                                sync_status=False, stream=None):
+    """lora_nf4_fwd without a workspace or any device allocation, for callers that may not
+    allocate: the split-K scratch is a 16 MiB static device buffer shared by all calls on a
+    device (calls that overlap on the GPU race).  Returns (Y, T)."""
+    torch = _torch()
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, n_out), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.bfloat16, device=X.device)
+    v = view(packed, n_out, k_in)
+    status = C.c_uint32(0)
+    check(lib.lora_nf4_fwd_static_scratch(C.byref(v), _p(X), M, _p(A), _p(B), r, float(scale), _p(residual),
+                                          _p(Y), _p(T), C.byref(status) if sync_status else None,
+                                          _stream(stream)))
+    return Y, T
+
+
 def lora_nf4_bwd(packed, n_out, k_in, X, T, dY, A, B, r, scale, dX=None, accumulate_dX=False, dA=None,
                  dB=None, ws=None, want_dX=True, stream=None):
     """dX (+)= dY W + dT A, dA = dT^T X, dB = s dY^T T with dT = bf16(s dY B).  Returns (dX, dA, dB)."""

@@ -30,6 +30,7 @@ SOURCES = [
     "layer_stack.cpp",
     "tc_gemm.cu",
     "elementwise.cu",
+    "lora_noalloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

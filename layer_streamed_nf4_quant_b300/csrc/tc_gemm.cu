@@ -729,7 +729,7 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     }
     p_.total_tiles = tiles;
     memcpy(p_.levels, nf4_levels(), sizeof(p_.levels));
-    p_.err = device_error_word();
+    p_.err = ext_err_ ? ext_err_ : device_error_word();
     if (!p_.err) return LSN_ECUDA;
 
     static bool attr_set[64] = {false};

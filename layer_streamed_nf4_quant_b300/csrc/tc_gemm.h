@@ -119,6 +119,9 @@ class GemmPlan {
     // Launches the GEMM and the split reductions (a dry plan only validates).
     int launch(cudaStream_t s, float* partial_ws, size_t ws_bytes);
     int status() const { return status_; }
+    // Device error word the kernel reports bounded-wait timeouts into (default: the
+    // library's lazily allocated per-device word).
+    void set_error_word(uint32_t* w) { ext_err_ = w; }
 
    private:
     GemmParams p_;
@@ -126,6 +129,7 @@ class GemmPlan {
     int map_box_[kMaxMaps] = {0};   // box rows of each map (the kernel's byte counts rely on it)
     int status_ = 0;
     bool dry_ = false;
+    uint32_t* ext_err_ = nullptr;
 };
 
 // Sums the split partials of EPI_PARTIAL problems in split order and applies the final
