@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/lsn.h"
+#include "lsn.h"
 
 namespace lsn {
 

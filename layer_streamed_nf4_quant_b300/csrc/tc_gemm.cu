@@ -30,14 +30,14 @@ namespace lsn {
 static_assert(sizeof(GemmParams) <= 32764, "kernel parameters must fit the 32 KB limit");
 
 constexpr int kDequantWarp0 = 8;
-constexpr int kDequantWarps = 8;
+constexpr int kDequantWarpsPerStep = 4;   // one of the two producer groups
 constexpr int kEpiWarp0 = 4;
 constexpr size_t kGemmSmemBytes =
-    1024 + (size_t)kStages * (kStageABytes + kStageBBytes) + 8 * (2 * kStages + 2) + 128;
+    1024 + (size_t)kStages * (kStageABytes + kStageBBytes) + 8 * (3 * kStages + 2) + 128;
 
 // Wait-site ids recorded in the device error word when a bounded wait runs out.
 enum : uint32_t { kSiteEmptyTma = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4,
-                  kSiteEmptyDeq = 5 };
+                  kSiteEmptyDeq = 5, kSitePeerFull = 6, kSiteRelay = 7 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -51,50 +51,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Decodes the 64 weights W[row][col0 .. col0+63] (exactly one absmax block) into 32 words of
-// packed bf16 pairs, element order preserved.  Each weight is bf16_rn(fp32(level * a')),
-// a' = fp32(fp32(q * scale) + offset).
-__device__ __forceinline__ void nf4_decode_block(const Nf4Dev& w, int64_t row, int64_t col0,
-                                                 const float* lv, uint32_t (&o)[32]) {
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// The raw bytes of one 64-weight NF4 block: its 32 code bytes, its absmax code and its
+// group's scale and offset.  Loaded one step ahead of the decode to hide memory latency.
+struct Nf4Block {
+    uint4 c0, c1;
+    uint32_t q;
+    float sc, off;
+};
+
+__device__ __forceinline__ void nf4_load_block(const Nf4Dev& w, int64_t row, int64_t col0, Nf4Block& b) {
     const int64_t e0 = row * w.k_in + col0;
     const int64_t blk = e0 >> 6;
     const uint4* src = reinterpret_cast<const uint4*>(w.codes + (e0 >> 1));
-    const uint4 c0 = __ldg(src);
-    const uint4 c1 = __ldg(src + 1);
-    const float q = (float)__ldg(w.absmax + blk);
+    b.c0 = __ldg(src);
+    b.c1 = __ldg(src + 1);
+    b.q = __ldg(w.absmax + blk);
     const int64_t g = blk >> 8;
-    const float a = __fadd_rn(__fmul_rn(q, __ldg(w.scale + g)), __ldg(w.offset + g));
-    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    b.sc = __ldg(w.scale + g);
+    b.off = __ldg(w.offset + g);
+}
+
+// Decodes one block into 32 words of packed bf16 pairs (element order preserved).  Every
+// weight is bf16_rn(fp32(level[code] * a')), a' = fp32(fp32(q * scale) + offset): the 16
+// possible values of the block are computed first, with exactly that rounding, and split
+// into a low-byte and a high-byte table (four registers each).  Each code then indexes the
+// tables with byte permutes: prmt picks entries 0-7 and 8-15 by the code's low three bits,
+// a sign-replicating prmt turns the code's top bit into a byte mask that selects between
+// them, and a final prmt interleaves low and high bytes into bf16 pairs.
+__device__ __forceinline__ void nf4_decode_regs(const Nf4Block& bk, const float (&lv)[16], uint32_t (&o)[32]) {
+    const float a = __fadd_rn(__fmul_rn((float)bk.q, bk.sc), bk.off);
+    uint32_t P[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) P[j] = pack_bf16x2(__fmul_rn(lv[2 * j], a), __fmul_rn(lv[2 * j + 1], a));
+    // byte k of L0..L3 / H0..H3: low / high byte of the value of code 4*i + k
+    const uint32_t L0 = prmt(P[0], P[1], 0x6420u), L1 = prmt(P[2], P[3], 0x6420u);
+    const uint32_t L2 = prmt(P[4], P[5], 0x6420u), L3 = prmt(P[6], P[7], 0x6420u);
+    const uint32_t H0 = prmt(P[0], P[1], 0x7531u), H1 = prmt(P[2], P[3], 0x7531u);
+    const uint32_t H2 = prmt(P[4], P[5], 0x7531u), H3 = prmt(P[6], P[7], 0x7531u);
+    const uint32_t wd[8] = {bk.c0.x, bk.c0.y, bk.c0.z, bk.c0.w, bk.c1.x, bk.c1.y, bk.c1.z, bk.c1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t b = (wd[i] >> (8 * j)) & 0xFFu;
-            // weight 2k sits in the high nibble of byte k
-            o[4 * i + j] = pack_bf16x2(__fmul_rn(lv[b >> 4], a), __fmul_rn(lv[b & 15u], a));
+        for (int h = 0; h < 2; ++h) {
+            // selector nibbles: codes of weights 1, 0, 3, 2 of this group of four
+            // (weight 2k sits in the high nibble of byte k)
+            const uint32_t S = h ? (wd[i] >> 16) : wd[i];
+            const uint32_t S7 = S & 0x7777u;
+            const uint32_t M = prmt(S << 4, S, 0xD9C8u);   // 0xFF where the code is >= 8
+            const uint32_t lo = (prmt(L0, L1, S7) & ~M) | (prmt(L2, L3, S7) & M);
+            const uint32_t hi = (prmt(H0, H1, S7) & ~M) | (prmt(H2, H3, S7) & M);
+            o[4 * i + 2 * h] = prmt(lo, hi, 0x4051u);       // weights 0, 1
+            o[4 * i + 2 * h + 1] = prmt(lo, hi, 0x6273u);   // weights 2, 3
         }
     }
 }
 
-__device__ __forceinline__ void smem_row_zero(uint32_t dst) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) st_shared_v4(dst + (ch << 4), 0u, 0u, 0u, 0u);
-}
-
-// Writes 32 words (64 bf16) as one 128-byte swizzled row: 16-byte chunk ch goes to chunk
-// position ch ^ swz, swz = row index within its 8-row (1024-byte) group.
-__device__ __forceinline__ void smem_row_store(uint32_t dst, uint32_t swz, const uint32_t (&o)[32]) {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(dst + ((ch ^ swz) << 4), o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
-}
-
-// One row of a dense bf16 matrix (k <= 64 elements, k % 8 == 0) times `scale`, zero padded.
-__device__ __forceinline__ void smem_row_scaled(uint32_t dst, uint32_t swz, const uint16_t* src,
-                                                int k, float scale) {
+// One row of a dense bf16 matrix (k <= 64 elements, k % 8 == 0) times `scale`, zero padded,
+// as 32 words of bf16 pairs.
+__device__ __forceinline__ void scaled_row(const uint16_t* src, int k, float scale, uint32_t (&o)[32]) {
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
         if (ch * 8 < k) {
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
             const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -102,35 +125,37 @@ __device__ __forceinline__ void smem_row_scaled(uint32_t dst, uint32_t swz, cons
             for (int j = 0; j < 4; ++j) {
                 const float lo = __uint_as_float(in[j] << 16);
                 const float hi = __uint_as_float(in[j] & 0xFFFF0000u);
-                o[j] = pack_bf16x2(__fmul_rn(lo, scale), __fmul_rn(hi, scale));
+                w[j] = pack_bf16x2(__fmul_rn(lo, scale), __fmul_rn(hi, scale));
             }
         }
-        st_shared_v4(dst + ((ch ^ swz) << 4), o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[4 * ch + j] = w[j];
     }
 }
 
 struct TileInfo {
     int prob, m0, n0, split, ks_begin, ks_end;
-    bool half1;
+    bool half0, half1;   // whether each 128-row half of this CTA's M tile holds any row
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, uint32_t rank) {
     int pi = 0;
     while (pi + 1 < p.n_probs && t >= p.probs[pi + 1].tile_begin) ++pi;
     const Problem& pr = p.probs[pi];
     const int l = t - pr.tile_begin;
-    const int per_split = pr.tiles_m * pr.tiles_n;
+    const int per_split = pr.tiles_m * pr.tiles_n;   // tiles_m counts M-pairs
     const int s = l / per_split;
     const int r = l - s * per_split;
     const int nt = r / pr.tiles_m;
     const int mt = r - nt * pr.tiles_m;
     TileInfo ti;
     ti.prob = pi;
-    ti.m0 = mt * kBM;
+    ti.m0 = (2 * mt + (int)rank) * kBM;
     ti.n0 = nt * pr.bn;
     ti.split = s;
     ti.ks_begin = (int)((int64_t)pr.ksteps * s / pr.splits);
     ti.ks_end = (int)((int64_t)pr.ksteps * (s + 1) / pr.splits);
+    ti.half0 = ti.m0 < pr.m;
     ti.half1 = ti.m0 + 128 < pr.m;
     return ti;
 }
@@ -149,6 +174,100 @@ __device__ __forceinline__ void locate(const GemmParams& p, const Problem& pr, i
 }
 
 __device__ __forceinline__ bool seg_b_mn(int b_src) { return b_src == B_NF4_MN || b_src == B_TMA_MN; }
+
+// Position in the cluster's flattened sequence of (tile, k-step); every role walks it.
+struct SeqPos {
+    int t;        // schedule tile (>= total_tiles: finished)
+    TileInfo ti;
+    int ks;       // problem-level k-step
+    int si, kk;   // segment and k-step within it
+};
+
+__device__ __forceinline__ void seq_tile(const GemmParams& p, SeqPos& s, uint32_t rank) {
+    if (s.t < p.total_tiles) {
+        s.ti = decode_tile(p, s.t, rank);
+        s.ks = s.ti.ks_begin;
+        locate(p, p.probs[s.ti.prob], s.ks, s.si, s.kk);
+    }
+}
+
+__device__ __forceinline__ void seq_begin(const GemmParams& p, SeqPos& s, uint32_t rank) {
+    s.t = (int)ptx::cluster_id_x();
+    seq_tile(p, s, rank);
+}
+
+__device__ __forceinline__ void seq_next(const GemmParams& p, SeqPos& s, uint32_t rank) {
+    if (s.t >= p.total_tiles) return;
+    if (++s.ks >= s.ti.ks_end) {
+        s.t += (int)ptx::n_clusters_x();
+        seq_tile(p, s, rank);
+        return;
+    }
+    if (++s.kk >= p.segs[s.si].ksteps) {
+        ++s.si;
+        s.kk = 0;
+    }
+}
+
+// What one B-producer thread writes for one k-step: one 128-byte row of this CTA's half of
+// the B tile.  A pair MMA takes N/2 of B's rows (K-major) or N/2 of its columns (MN-major,
+// in whole 64-column atoms) from each CTA's shared memory at the same offset.
+enum : int { kJobNone = 0, kJobNf4 = 1, kJobZero = 2, kJobScaled = 3 };
+struct DeqJob {
+    int kind;
+    int w;              // NF4 matrix index
+    int64_t row, col0;  // the block W[row][col0 .. col0+63]
+    uint32_t dst_off;   // byte offset of the 128-byte row within the stage's B half-tile
+    uint32_t swz;       // swizzle phase of that row
+    const uint16_t* sp; // kJobScaled: source row, its length and the factor
+    int sk;
+    float ss;
+};
+
+// j: row job within this CTA's half of the B tile, 0 .. bn/2 - 1.
+__device__ __forceinline__ DeqJob make_deq_job(const GemmParams& p, const SeqPos& s, int j, uint32_t rank) {
+    DeqJob d{};
+    d.kind = kJobNone;
+    const Problem& pr = p.probs[s.ti.prob];
+    const int half = pr.bn >> 1;
+    if (j >= half) return d;
+    const KSeg& sg = p.segs[s.si];
+    const int kk = s.kk;
+    const int nb = s.ti.n0 + (int)rank * half;   // first output column of this CTA's half
+    if (sg.b_src == B_NF4_K) {
+        const Nf4Dev& w = p.nf4[sg.b_idx];
+        d.w = sg.b_idx;
+        d.row = (int64_t)sg.b_n0 + nb + j;
+        d.col0 = (int64_t)sg.b_k0 + (int64_t)kk * kBK;
+        d.dst_off = j * 128;
+        d.swz = j & 7;
+        d.kind = (d.row < w.n_out && d.col0 < w.k_in) ? kJobNf4 : kJobZero;
+    } else if (sg.b_src == B_NF4_MN) {
+        const int r = j & 63;      // contraction row within the k-step
+        const int a = j >> 6;      // local 64-column atom
+        const Nf4Dev& w = p.nf4[sg.b_idx];
+        const int kin = kk * kBK + r;
+        d.w = sg.b_idx;
+        d.row = (int64_t)sg.b_k0 + kin;
+        d.col0 = (int64_t)sg.b_n0 + nb + 64 * a;
+        d.dst_off = a * 8192 + r * 128;
+        d.swz = r & 7;
+        d.kind = (kin < sg.k_len && d.row < w.n_out && d.col0 < w.k_in) ? kJobNf4 : kJobZero;
+    } else if (sg.b_src == B_SCALED_K) {
+        const int64_t n = (int64_t)nb + j;
+        d.dst_off = j * 128;
+        d.swz = j & 7;
+        if (n < sg.b_rows) {
+            d.kind = kJobScaled;
+            d.sp = sg.b_ptr + n * sg.b_ld;
+            d.sk = sg.k_len;
+            d.ss = sg.b_scale;
+        } else {
+            d.kind = kJobZero;
+        }
+    }
+    return d;
+}
 
 // ----------------------------------------------------------------------------- epilogue
 
@@ -232,126 +351,157 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     const uint32_t sB = base + kStages * kStageABytes;
     const uint32_t sBar = sB + kStages * kStageBBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
-    auto empty_bar = [&](int s) { return sBar + 8u * (kStages + s); };
-    const uint32_t acc_full = sBar + 8u * (2 * kStages);
+    auto pfull_bar = [&](int s) { return sBar + 8u * (kStages + s); };
+    auto empty_bar = [&](int s) { return sBar + 8u * (2 * kStages + s); };
+    const uint32_t acc_full = sBar + 8u * (3 * kStages);
     const uint32_t acc_empty = acc_full + 8u;
-    uint8_t* const gmisc = gbase + (sBar - base) + 8 * (2 * kStages + 2);
+    uint8_t* const gmisc = gbase + (sBar - base) + 8 * (3 * kStages + 2);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc + 4);
-    float* const lv = reinterpret_cast<float*>(gmisc + 64);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();   // 0 (issues the pair MMAs) or 1
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(full_bar(s), 1 + kDequantWarps);
-            ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(full_bar(s), 1 + kDequantWarpsPerStep);   // own TMA + own producer group
+            ptx::mbar_init(pfull_bar(s), 1);                         // the peer's stage is full
+            ptx::mbar_init(empty_bar(s), 1);                         // the pair MMAs read the stage
         }
         ptx::mbar_init(acc_full, 1);
-        ptx::mbar_init(acc_empty, 128);
+        ptx::mbar_init(acc_empty, 256);   // both CTAs' epilogue threads (used in the even CTA)
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (threadIdx.x < 16) lv[threadIdx.x] = p.levels[threadIdx.x];
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
+        ptx::tmem_relinquish_pair();
     }
     __syncthreads();
+    ptx::cluster_sync();   // both CTAs' barriers are initialised before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-                const TileInfo ti = decode_tile(p, t);
-                const Problem& pr = p.probs[ti.prob];
-                for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
-                    if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err,
-                                                kSiteEmptyTma))
-                        goto tma_done;
-                    int si, kk;
-                    locate(p, pr, ks, si, kk);
-                    const KSeg& sg = p.segs[si];
-                    const uint32_t bar = full_bar(stage);
-                    const uint32_t a_dst = sA + stage * kStageABytes;
-                    const uint32_t b_dst = sB + stage * kStageBBytes;
-                    uint32_t bytes = kStageABytes;
-                    if (sg.b_src == B_TMA_K || sg.b_src == B_TMA_MN) bytes += pr.bn * kBK * 2;
-                    ptx::mbar_arrive_expect_tx(bar, bytes);
-                    const int ak = sg.a_k0 + kk * kBK;
-                    if (pr.a_major == A_KMAJOR) {
-                        ptx::tma_load_2d(a_dst, &p.maps[sg.a_map], ak, ti.m0, bar);
-                    } else {
+            SeqPos s;
+            seq_begin(p, s, rank);
+            uint32_t n_steps = 0;
+            for (uint32_t i = 0; s.t < p.total_tiles; ++i, seq_next(p, s, rank)) {
+                const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+                if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyTma))
+                    break;
+                const Problem& pr = p.probs[s.ti.prob];
+                const KSeg& sg = p.segs[s.si];
+                const int half = pr.bn >> 1;
+                const uint32_t bar = full_bar(stage);
+                const uint32_t a_dst = sA + stage * kStageABytes;
+                const uint32_t b_dst = sB + stage * kStageBBytes;
+                uint32_t bytes = kStageABytes;
+                if (sg.b_src == B_TMA_K || sg.b_src == B_TMA_MN) bytes += half * kBK * 2;
+                ptx::mbar_arrive_expect_tx(bar, bytes);
+                const int ak = sg.a_k0 + s.kk * kBK;
+                if (pr.a_major == A_KMAJOR) {
+                    ptx::tma_load_2d(a_dst, &p.maps[sg.a_map], ak, s.ti.m0, bar);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < kBM / 64; ++i)
-                            ptx::tma_load_2d(a_dst + i * 8192, &p.maps[sg.a_map], ti.m0 + 64 * i, ak, bar);
-                    }
-                    const int bk = sg.b_k0 + kk * kBK;
-                    if (sg.b_src == B_TMA_K) {
-                        ptx::tma_load_2d(b_dst, &p.maps[sg.b_idx], bk, sg.b_n0 + ti.n0, bar);
-                    } else if (sg.b_src == B_TMA_MN) {
-                        for (int i = 0; i < pr.bn / 64; ++i)
-                            ptx::tma_load_2d(b_dst + i * 8192, &p.maps[sg.b_idx], sg.b_n0 + ti.n0 + 64 * i,
-                                             bk, bar);
-                    }
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    for (int q = 0; q < kBM / 64; ++q)
+                        ptx::tma_load_2d(a_dst + q * 8192, &p.maps[sg.a_map], s.ti.m0 + 64 * q, ak, bar);
+                }
+                const int bk = sg.b_k0 + s.kk * kBK;
+                const int nb = sg.b_n0 + s.ti.n0 + (int)rank * half;
+                if (sg.b_src == B_TMA_K) {
+                    ptx::tma_load_2d(b_dst, &p.maps[sg.b_idx], bk, nb, bar);
+                } else if (sg.b_src == B_TMA_MN) {
+                    for (int q = 0; q < half / 64; ++q)
+                        ptx::tma_load_2d(b_dst + q * 8192, &p.maps[sg.b_idx], nb + 64 * q, bk, bar);
+                }
+                n_steps = i + 1;
+            }
+            // Wait for the last release of every stage: the pair MMAs' commits arrive on this
+            // CTA's empty barriers asynchronously, and they must land before the CTA exits.
+            if (!*abort_flag) {
+                for (uint32_t st = 0; st < (uint32_t)kStages && st < n_steps; ++st) {
+                    const uint32_t last = st + ((n_steps - 1 - st) / kStages) * kStages;
+                    if (!ptx::mbar_wait_bounded(empty_bar(st), (last / kStages) & 1u, abort_flag, p.err,
+                                                kSiteEmptyTma))
+                        break;
                 }
             }
-        tma_done:;
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ UMMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc_phase = 0;
-            for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-                const TileInfo ti = decode_tile(p, t);
+        // ------------------------------------------------------ pair UMMA issuer (rank 0)
+        if (lane == 0 && leader) {
+            SeqPos s;
+            seq_begin(p, s, rank);
+            uint32_t acc_phase = 0;
+            uint32_t i = 0;
+            while (s.t < p.total_tiles) {
+                const int t = s.t;
+                const TileInfo ti = s.ti;
                 const Problem& pr = p.probs[ti.prob];
                 if (!ptx::mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, p.err, kSiteAccEmpty))
                     break;
                 ptx::tc_fence_after();
                 const bool a_mn = pr.a_major == A_MNMAJOR;
-                for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
-                    if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteFull))
-                        goto mma_done;
+                bool ok = true;
+                for (; s.t == t; ++i, seq_next(p, s, rank)) {
+                    const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+                    if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteFull) ||
+                        !ptx::mbar_wait_bounded(pfull_bar(stage), phase, abort_flag, p.err, kSitePeerFull)) {
+                        ok = false;
+                        break;
+                    }
                     ptx::tc_fence_after();
-                    int si, kk;
-                    locate(p, pr, ks, si, kk);
-                    const bool b_mn = seg_b_mn(p.segs[si].b_src);
-                    const uint32_t idesc = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, b_mn ? 1 : 0);
+                    const bool b_mn = seg_b_mn(p.segs[s.si].b_src);
+                    const uint32_t idesc = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, b_mn ? 1 : 0, 256);
                     const uint32_t a_base = sA + stage * kStageABytes;
                     const uint32_t b_base = sB + stage * kStageBBytes;
 #pragma unroll
                     for (int k4 = 0; k4 < kBK / 16; ++k4) {
                         const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(b_base + k4 * 2048, 8192, 1024)
                                                     : ptx::smem_desc_sw128(b_base + k4 * 32, 16, 1024);
-                        const uint32_t acc = (ks > ti.ks_begin || k4 > 0) ? 1u : 0u;
+                        const uint32_t acc = (s.ks > ti.ks_begin || k4 > 0) ? 1u : 0u;
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            if (h == 1 && !ti.half1) break;
+                            // rows of block h: 128 of this CTA's tile and 128 of the peer's
+                            if ((h == 0 && !ti.half0) || (h == 1 && !ti.half1)) continue;
                             const uint32_t ab = a_base + h * (kStageABytes / 2);
                             const uint64_t adesc = a_mn ? ptx::smem_desc_sw128(ab + k4 * 2048, 8192, 1024)
                                                         : ptx::smem_desc_sw128(ab + k4 * 32, 16, 1024);
-                            ptx::umma_f16(tmem + (uint32_t)(h * pr.bn), adesc, bdesc, idesc, acc);
+                            ptx::umma_f16_pair(tmem + (uint32_t)(h * pr.bn), adesc, bdesc, idesc, acc);
                         }
                     }
-                    ptx::umma_commit(empty_bar(stage));
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    ptx::umma_commit_pair_mc(empty_bar(stage), 0x3);
                 }
-                ptx::umma_commit(acc_full);
+                if (!ok) break;
+                ptx::umma_commit_pair_mc(acc_full, 0x3);
                 acc_phase ^= 1u;
             }
-        mma_done:;
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------- relay of stage readiness (rank 1)
+        if (lane == 0 && !leader) {
+            const uint32_t remote_pfull0 = ptx::mapa(pfull_bar(0), 0);
+            SeqPos s;
+            seq_begin(p, s, rank);
+            for (uint32_t i = 0; s.t < p.total_tiles; ++i, seq_next(p, s, rank)) {
+                const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+                if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteRelay)) break;
+                ptx::mbar_arrive_remote(remote_pfull0 + 8u * stage);
+            }
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------------- epilogue
         const int q = warp - kEpiWarp0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile(p, t);
+        const uint32_t acc_empty_dst = leader ? acc_empty : ptx::mapa(acc_empty, 0);
+        for (int t = (int)ptx::cluster_id_x(); t < p.total_tiles; t += (int)ptx::n_clusters_x()) {
+            const TileInfo ti = decode_tile(p, t, rank);
+            const TileInfo t0 = decode_tile(p, t, 0);   // which blocks the pair MMAs wrote
             const Problem& pr = p.probs[ti.prob];
             int ok = 0;
             if (lane == 0) ok = ptx::mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.err, kSiteAccFull);
@@ -359,7 +509,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             if (!ok) break;
             ptx::tc_fence_after();
             for (int h = 0; h < 2; ++h) {
-                if (h == 1 && !ti.half1) break;
+                if ((h == 0 && !t0.half0) || (h == 1 && !t0.half1)) continue;
                 const int row = ti.m0 + h * 128 + q * 32 + lane;
                 for (int c = 0; c < pr.bn; c += 32) {
                     float v[32];
@@ -368,76 +518,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(acc_empty);
+            if (leader) ptx::mbar_arrive(acc_empty_dst);
+            else ptx::mbar_arrive_remote(acc_empty_dst);
             acc_phase ^= 1u;
         }
     } else if (warp >= kDequantWarp0) {
         // --------------------------------------------------------------- B producer
+        // Two groups of four warps take alternate k-steps of the sequence, so two k-steps
+        // are being decoded at once; each thread owns one 128-byte row of this CTA's half of
+        // the B tile.
         const int dt = threadIdx.x - kDequantWarp0 * 32;   // 0 .. 255
-        uint32_t stage = 0, phase = 0;
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile(p, t);
-            const Problem& pr = p.probs[ti.prob];
-            for (int ks = ti.ks_begin; ks < ti.ks_end; ++ks) {
-                int ok = 0;
-                if (lane == 0)
-                    ok = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) goto deq_done;
-                {
-                    int si, kk;
-                    locate(p, pr, ks, si, kk);
-                    const KSeg& sg = p.segs[si];
-                    const uint32_t b_dst = sB + stage * kStageBBytes;
-                    if (sg.b_src == B_NF4_K) {
-                        if (dt < pr.bn) {
-                            const Nf4Dev& w = p.nf4[sg.b_idx];
-                            const int64_t wrow = (int64_t)sg.b_n0 + ti.n0 + dt;
-                            const int64_t col0 = (int64_t)sg.b_k0 + (int64_t)kk * kBK;
-                            const uint32_t dst = b_dst + dt * 128;
-                            if (wrow < w.n_out && col0 < w.k_in) {
-                                uint32_t o[32];
-                                nf4_decode_block(w, wrow, col0, lv, o);
-                                smem_row_store(dst, dt & 7, o);
-                            } else {
-                                smem_row_zero(dst);
-                            }
-                        }
-                    } else if (sg.b_src == B_NF4_MN) {
-                        const int j = dt & 63;
-                        const int a = dt >> 6;
-                        if (a < pr.bn / 64) {
-                            const Nf4Dev& w = p.nf4[sg.b_idx];
-                            const int kin = kk * kBK + j;
-                            const int64_t wrow = (int64_t)sg.b_k0 + kin;
-                            const int64_t col0 = (int64_t)sg.b_n0 + ti.n0 + 64 * a;
-                            const uint32_t dst = b_dst + a * 8192 + j * 128;
-                            if (kin < sg.k_len && wrow < w.n_out && col0 < w.k_in) {
-                                uint32_t o[32];
-                                nf4_decode_block(w, wrow, col0, lv, o);
-                                smem_row_store(dst, j & 7, o);
-                            } else {
-                                smem_row_zero(dst);
-                            }
-                        }
-                    } else if (sg.b_src == B_SCALED_K) {
-                        if (dt < pr.bn) {
-                            const int64_t n = (int64_t)ti.n0 + dt;
-                            const uint32_t dst = b_dst + dt * 128;
-                            if (n < sg.b_rows)
-                                smem_row_scaled(dst, dt & 7, sg.b_ptr + n * sg.b_ld, sg.k_len, sg.b_scale);
-                            else
-                                smem_row_zero(dst);
-                        }
-                    }
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(full_bar(stage));
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
-            }
+        const int grp = dt >> 7;
+        const int gt = dt & 127;
+        SeqPos s;
+        seq_begin(p, s, rank);
+        uint32_t i = 0;
+        if (grp == 1) {
+            seq_next(p, s, rank);
+            i = 1;
         }
-    deq_done:;
+        DeqJob cur{};
+        Nf4Block cb{};
+        if (s.t < p.total_tiles) {
+            cur = make_deq_job(p, s, gt, rank);
+            if (cur.kind == kJobNf4) nf4_load_block(p.nf4[cur.w], cur.row, cur.col0, cb);
+        }
+        while (s.t < p.total_tiles) {
+            SeqPos sn = s;
+            seq_next(p, sn, rank);
+            seq_next(p, sn, rank);
+            DeqJob nxt{};
+            Nf4Block nb{};
+            if (sn.t < p.total_tiles) {
+                nxt = make_deq_job(p, sn, gt, rank);
+                if (nxt.kind == kJobNf4) nf4_load_block(p.nf4[nxt.w], nxt.row, nxt.col0, nb);
+            }
+            const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+            int ok = 0;
+            if (lane == 0)
+                ok = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (cur.kind != kJobNone) {
+                const uint32_t dst = sB + stage * kStageBBytes + cur.dst_off;
+                uint32_t o[32];
+                if (cur.kind == kJobNf4) {
+                    nf4_decode_regs(cb, p.levels, o);
+                } else if (cur.kind == kJobScaled) {
+                    scaled_row(cur.sp, cur.sk, cur.ss, o);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = 0u;
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(dst + (uint32_t)((ch ^ (int)cur.swz) << 4), o[4 * ch], o[4 * ch + 1],
+                                 o[4 * ch + 2], o[4 * ch + 3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(full_bar(stage));
+            cur = nxt;
+            cb = nb;
+            s = sn;
+            i += 2;
+        }
     }
 
     __syncthreads();
@@ -446,9 +591,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         if (threadIdx.x == 0) ptx::settle_ns(50000);
         __syncthreads();
     }
+    ptx::cluster_sync();   // no CTA leaves while the pair may still use its memory
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 512);
+        ptx::tmem_dealloc_pair(tmem, 512);
     }
 }
 
@@ -507,16 +653,15 @@ __global__ void gemm_reduce_kernel(const float* __restrict__ partial, int splits
 // --------------------------------------------------------------------- dequant (tests)
 
 __global__ void nf4_dequant_kernel(Nf4Dev w, Nf4Levels lvl, uint16_t* __restrict__ out) {
-    __shared__ float lv[16];
-    if (threadIdx.x < 16) lv[threadIdx.x] = lvl.v[threadIdx.x];
-    __syncthreads();
     const int64_t nb = w.n_out * (w.k_in / 64);
     for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nb;
          b += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = b / (w.k_in / 64);
         const int64_t col0 = (b - row * (w.k_in / 64)) * 64;
+        Nf4Block bk;
+        nf4_load_block(w, row, col0, bk);
         uint32_t o[32];
-        nf4_decode_block(w, row, col0, lv, o);
+        nf4_decode_regs(bk, lvl.v, o);
         uint4* dst = reinterpret_cast<uint4*>(out + row * w.k_in + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
@@ -556,6 +701,38 @@ int num_sms() {
         sms[dev] = v;
     }
     return sms[dev];
+}
+
+// Largest number of CTA pairs of the GEMM kernel that can be resident at once (per device).
+static int max_pair_clusters() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev]) return cached[dev];
+    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes) !=
+        cudaSuccess) {
+        fail(LSN_ECUDA, "cudaFuncSetAttribute(max dynamic shared memory) failed");
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * 74, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel, &cfg);
+    if (e != cudaSuccess || n < 1) {
+        fail(LSN_ECUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+        return 0;
+    }
+    cached[dev] = n;
+    return n;
 }
 
 int choose_splits(int64_t tiles, int ksteps) {
@@ -616,7 +793,8 @@ int GemmPlan::problem(int m, int n, int bn, int a_major, int epi, void* out, int
                       int n_valid, int splits, const uint16_t* residual, int64_t ldr) {
     if (status_) return -1;
     if (p_.n_probs >= kMaxProbs) return status_ = fail(LSN_EINVAL, "gemm: too many problems");
-    if (m < 1 || n < 1 || !(bn == 64 || bn == 128 || bn == 256) || (!out && !dry_) || n_valid < 1 ||
+    if (bn < kMinBN) bn = kMinBN;   // a pair MMA needs at least one 64-wide atom per CTA
+    if (m < 1 || n < 1 || !(bn == 128 || bn == 256) || (!out && !dry_) || n_valid < 1 ||
         n_valid > n || n_valid % 8 || splits < 1 || (reinterpret_cast<uintptr_t>(out) & 15))
         return status_ = fail(LSN_EINVAL, "gemm: bad problem");
     Problem& pr = p_.probs[p_.n_probs];
@@ -649,8 +827,8 @@ int GemmPlan::seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0,
         const Problem& pr = p_.probs[p_.n_probs - 1];
         const int want_a = pr.a_major == A_KMAJOR ? kBM : 64;
         if (map_box_[a_map] != want_a) return status_ = fail(LSN_EINVAL, "gemm: A map box rows mismatch");
-        if (b_src == B_TMA_K && map_box_[b_idx] != pr.bn)
-            return status_ = fail(LSN_EINVAL, "gemm: K-major B map box rows must equal the N tile");
+        if (b_src == B_TMA_K && map_box_[b_idx] != pr.bn / 2)
+            return status_ = fail(LSN_EINVAL, "gemm: K-major B map box rows must be half the N tile");
         if (b_src == B_TMA_MN && map_box_[b_idx] != 64)
             return status_ = fail(LSN_EINVAL, "gemm: MN-major B map box rows must be 64");
     }
@@ -710,7 +888,7 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
         Problem& pr = p_.probs[i];
         if (pr.seg_count == 0) return status_ = fail(LSN_EINVAL, "gemm: problem without segments");
         if (pr.splits > pr.ksteps) pr.splits = pr.ksteps;
-        pr.tiles_m = (pr.m + kBM - 1) / kBM;
+        pr.tiles_m = ((pr.m + kBM - 1) / kBM + 1) / 2;   // M-pairs: one per CTA pair
         pr.tiles_n = (pr.n + pr.bn - 1) / pr.bn;
         pr.tile_begin = tiles;
         tiles += pr.tiles_m * pr.tiles_n * pr.splits;
@@ -732,17 +910,23 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     p_.err = ext_err_ ? ext_err_ : device_error_word();
     if (!p_.err) return LSN_ECUDA;
 
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        LSN_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)kGemmSmemBytes));
-        attr_set[dev] = true;
-    }
-    const int grid = tiles < num_sms() ? tiles : num_sms();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = max_pair_clusters();
+    if (clusters < 1) return status_ = LSN_ECUDA;
+    if (tiles < clusters) clusters = tiles;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
     void* prof = profile_begin(s);
-    tc_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, s>>>(p_);
+    LSN_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_gemm_kernel, p_));
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     if (prof) {

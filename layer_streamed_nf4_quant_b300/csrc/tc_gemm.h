@@ -16,12 +16,13 @@
 
 namespace lsn {
 
-constexpr int kBM = 256;        // rows per tile: two M=128 UMMA halves share each B tile
+constexpr int kBM = 256;        // rows per CTA tile: two 128-row blocks, each half of a pair MMA
 constexpr int kBK = 64;         // contraction per stage: one NF4 block, one 128-byte row
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
+constexpr int kMinBN = 128;     // a pair MMA splits B's N over the two CTAs in 64-wide atoms
 constexpr int kStageABytes = kBM * kBK * 2;
-constexpr int kStageBBytes = kMaxBN * kBK * 2;
+constexpr int kStageBBytes = (kMaxBN / 2) * kBK * 2;   // this CTA's half of the B tile
 constexpr int kGemmThreads = 512;
 constexpr int kMaxMaps = 16;
 constexpr int kMaxNf4 = 8;
