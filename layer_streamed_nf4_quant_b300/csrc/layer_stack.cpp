@@ -32,7 +32,7 @@ namespace {
 
 inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
-inline int tiles_of(int64_t m, int64_t n, int bn) { return ceil_div(m, kBM) * ceil_div(n, bn); }
+inline int tiles_of(int64_t m, int64_t n, int bn) { return pair_tiles(m, n, bn); }
 
 struct Dims {
     int L, D, dkv, F, r, M, Ncat;

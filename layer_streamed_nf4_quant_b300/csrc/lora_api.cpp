@@ -13,9 +13,7 @@ namespace lsn {
 
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 static inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-static inline int tiles_of(int64_t m, int64_t n, int bn) {
-    return (int)(((m + kBM - 1) / kBM) * ((n + bn - 1) / bn));
-}
+static inline int tiles_of(int64_t m, int64_t n, int bn) { return pair_tiles(m, n, bn); }
 static inline int bn_for(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 static inline int ksteps_of(int64_t k) { return (int)((k + kBK - 1) / kBK); }
 

@@ -82,8 +82,8 @@ extern "C" int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X,
     const int K = (int)W->k_in, N = (int)W->n_out, m = (int)M;
     // the same split decisions as lora_nf4_fwd, so both give the same bits
     const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-    const int tiles_t = (int)((M + kBM - 1) / kBM);
-    const int tiles_y = tiles_t * ((N + bn - 1) / bn);
+    const int tiles_t = pair_tiles(M, r, 64);
+    const int tiles_y = pair_tiles(M, N, bn);
     const int st = choose_splits(tiles_t, (K + kBK - 1) / kBK);
     const int sy = choose_splits(tiles_y, (K + kBK - 1) / kBK + 1);
     const size_t need_t = partial_bytes(st, M, r), need_y = partial_bytes(sy, M, N);

@@ -29,6 +29,7 @@ namespace lsn {
 
 static_assert(sizeof(GemmParams) <= 32764, "kernel parameters must fit the 32 KB limit");
 
+constexpr int kRasterGroup = 8;   // M-pairs per raster group (8 x 512 rows of A)
 constexpr int kDequantWarp0 = 8;
 constexpr int kDequantWarpsPerStep = 4;   // one of the two producer groups
 constexpr int kEpiWarp0 = 4;
@@ -146,8 +147,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, uint
     const int per_split = pr.tiles_m * pr.tiles_n;   // tiles_m counts M-pairs
     const int s = l / per_split;
     const int r = l - s * per_split;
-    const int nt = r / pr.tiles_m;
-    const int mt = r - nt * pr.tiles_m;
+    // grouped raster: kRasterGroup M-pairs sweep all N tiles together, so the A rows of the
+    // group stay in L2 while B streams past them once per group
+    const int g = r / (kRasterGroup * pr.tiles_n);
+    const int first_m = g * kRasterGroup;
+    const int gm = min(kRasterGroup, pr.tiles_m - first_m);
+    const int rr = r - g * kRasterGroup * pr.tiles_n;
+    const int nt = rr / gm;
+    const int mt = first_m + (rr - nt * gm);
     TileInfo ti;
     ti.prob = pi;
     ti.m0 = (2 * mt + (int)rank) * kBM;
@@ -600,32 +607,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
 
 // ----------------------------------------------------------------------- split reduce
 
-__global__ void gemm_reduce_kernel(const float* __restrict__ partial, int splits, int m, int n,
-                                   int64_t part_stride, int epi, void* out, int64_t ldo, float alpha,
-                                   const uint16_t* __restrict__ residual, int64_t ldr, int n_valid) {
-    const int n4 = n_valid / 4;
-    const int64_t total = (int64_t)m * n4;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+struct ReduceJob {
+    const float* partial;
+    void* out;
+    const uint16_t* residual;
+    int64_t part_stride, ldo, ldr;
+    int splits, m, n, epi, n_valid;
+    float alpha;
+    int64_t begin;   // first work item of this job in the launch
+};
+constexpr int kMaxReduceJobs = kMaxProbs;
+struct ReduceJobs {
+    ReduceJob j[kMaxReduceJobs];
+    int count;
+    int64_t total;
+};
+
+// Sums the split partials of every split problem of one GEMM launch in split order and
+// applies each problem's final epilogue (four columns per work item).
+__global__ void gemm_reduce_kernel(const __grid_constant__ ReduceJobs jobs) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < jobs.total;
          idx += (int64_t)gridDim.x * blockDim.x) {
+        int k = 0;
+        while (k + 1 < jobs.count && idx >= jobs.j[k + 1].begin) ++k;
+        const ReduceJob& jb = jobs.j[k];
+        const int64_t local = idx - jb.begin;
+        const int n4 = jb.n_valid / 4;
         int row, c4;
-        if (epi == EPI_F32_T) {   // consecutive threads on consecutive rows: coalesced stores
-            c4 = (int)(idx / m);
-            row = (int)(idx - (int64_t)c4 * m);
+        if (jb.epi == EPI_F32_T) {   // consecutive threads on consecutive rows: coalesced stores
+            c4 = (int)(local / jb.m);
+            row = (int)(local - (int64_t)c4 * jb.m);
         } else {
-            row = (int)(idx / n4);
-            c4 = (int)(idx - (int64_t)row * n4);
+            row = (int)(local / n4);
+            c4 = (int)(local - (int64_t)row * n4);
         }
         const int col = c4 * 4;
-        const float* src = partial + (int64_t)row * n + col;
+        const float* src = jb.partial + (int64_t)row * jb.n + col;
         float4 acc = *reinterpret_cast<const float4*>(src);
-        for (int s = 1; s < splits; ++s) {
-            const float4 y = *reinterpret_cast<const float4*>(src + (int64_t)s * part_stride);
+        for (int s = 1; s < jb.splits; ++s) {
+            const float4 y = *reinterpret_cast<const float4*>(src + (int64_t)s * jb.part_stride);
             acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
         }
-        float f[4] = {acc.x * alpha, acc.y * alpha, acc.z * alpha, acc.w * alpha};
-        if (epi == EPI_BF16) {
-            if (residual) {
-                const uint2 r2 = *reinterpret_cast<const uint2*>(residual + (int64_t)row * ldr + col);
+        float f[4] = {acc.x * jb.alpha, acc.y * jb.alpha, acc.z * jb.alpha, acc.w * jb.alpha};
+        if (jb.epi == EPI_BF16) {
+            if (jb.residual) {
+                const uint2 r2 = *reinterpret_cast<const uint2*>(jb.residual + (int64_t)row * jb.ldr + col);
                 f[0] += __uint_as_float(r2.x << 16);
                 f[1] += __uint_as_float(r2.x & 0xFFFF0000u);
                 f[2] += __uint_as_float(r2.y << 16);
@@ -634,14 +660,14 @@ __global__ void gemm_reduce_kernel(const float* __restrict__ partial, int splits
             uint2 w;
             w.x = pack_bf16x2(f[0], f[1]);
             w.y = pack_bf16x2(f[2], f[3]);
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + (int64_t)row * ldo + col) = w;
-        } else if (epi == EPI_F32_T) {
-            float* o = static_cast<float*>(out);
-            for (int j = 0; j < 4; ++j) o[(int64_t)(col + j) * ldo + row] = f[j];
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(jb.out) + (int64_t)row * jb.ldo + col) = w;
+        } else if (jb.epi == EPI_F32_T) {
+            float* o = static_cast<float*>(jb.out);
+            for (int j = 0; j < 4; ++j) o[(int64_t)(col + j) * jb.ldo + row] = f[j];
         } else {
-            float* o = static_cast<float*>(out) + (int64_t)row * ldo + col;
+            float* o = static_cast<float*>(jb.out) + (int64_t)row * jb.ldo + col;
             float4 x = make_float4(f[0], f[1], f[2], f[3]);
-            if (epi == EPI_F32_ACC) {
+            if (jb.epi == EPI_F32_ACC) {
                 const float4 y = *reinterpret_cast<const float4*>(o);
                 x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
             }
@@ -669,6 +695,8 @@ __global__ void nf4_dequant_kernel(Nf4Dev w, Nf4Levels lvl, uint16_t* __restrict
 }
 
 // =========================================================================== host side
+
+static int launch_reduce(const ReduceJobs& jobs, cudaStream_t s);
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -735,13 +763,13 @@ static int max_pair_clusters() {
     return n;
 }
 
-int choose_splits(int64_t tiles, int ksteps) {
-    const int64_t kPlanSMs = 148;
-    if (tiles >= kPlanSMs || ksteps <= 1) return 1;
-    int64_t s = (kPlanSMs + tiles - 1) / tiles;
-    if (s > ksteps) s = ksteps;
+int choose_splits(int64_t units, int ksteps) {
+    const int64_t kTarget = 222;   // three waves of the 74 CTA pairs of a 148-SM part
+    if (units >= kTarget || ksteps < 4) return 1;
+    int64_t s = (kTarget + units - 1) / units;
+    if (s > ksteps / 2) s = ksteps / 2;
     if (s > 32) s = 32;
-    return (int)s;
+    return s < 1 ? 1 : (int)s;
 }
 
 GemmPlan::GemmPlan(bool dry) : dry_(dry) { memset(&p_, 0, sizeof(p_)); }
@@ -939,27 +967,37 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
         }
         profile_end(prof, s, flops);
     }
+    ReduceJobs jobs;
+    memset(&jobs, 0, sizeof(jobs));
     for (int i = 0; i < p_.n_probs; ++i) {
         const Problem& pr = p_.probs[i];
         if (pr.epi != EPI_PARTIAL) continue;
-        int rc = gemm_reduce(static_cast<const float*>(pr.out), pr.splits, pr.m, pr.n, pr.part_stride,
-                             fin[i].epi, fin[i].out, fin[i].ldo, fin[i].alpha, fin[i].res, fin[i].ldr,
-                             pr.n_valid, s);
-        if (rc) return rc;
+        ReduceJob& j = jobs.j[jobs.count++];
+        j.partial = static_cast<const float*>(pr.out);
+        j.out = fin[i].out;
+        j.residual = fin[i].res;
+        j.part_stride = pr.part_stride;
+        j.ldo = fin[i].ldo;
+        j.ldr = fin[i].ldr;
+        j.splits = pr.splits;
+        j.m = pr.m;
+        j.n = pr.n;
+        j.epi = fin[i].epi;
+        j.n_valid = pr.n_valid;
+        j.alpha = fin[i].alpha;
+        j.begin = jobs.total;
+        jobs.total += (int64_t)pr.m * (pr.n_valid / 4);
     }
-    return LSN_OK;
+    return launch_reduce(jobs, s);
 }
 
-int gemm_reduce(const float* partial, int splits, int m, int n, int64_t part_stride, int epi, void* out,
-                int64_t ldo, float alpha, const uint16_t* residual, int64_t ldr, int n_valid,
-                cudaStream_t s) {
-    const int64_t total = (int64_t)m * (n_valid / 4);
-    int64_t blocks = (total + 255) / 256;
+static int launch_reduce(const ReduceJobs& jobs, cudaStream_t s) {
+    if (jobs.count == 0) return LSN_OK;
+    int64_t blocks = (jobs.total + 255) / 256;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    gemm_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(partial, splits, m, n, part_stride, epi, out, ldo,
-                                                        alpha, residual, ldr, n_valid);
+    gemm_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(jobs);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;

@@ -7,7 +7,7 @@
 // swizzled shared-memory operand layout (K-major for y = x W^T, MN-major for dX = dY W), or
 // is loaded and scaled by the producer warps (the LoRA B factor times s).  Accumulation is
 // fp32 in TMEM; the epilogue writes bf16, fp32, fp32 added into the output, fp32 transposed,
-// or fp32 split-K partials that gemm_reduce sums in a fixed order.
+// or fp32 split-K partials that one reduction launch per GEMM launch sums in a fixed order.
 #pragma once
 
 #include <cuda.h>
@@ -133,17 +133,19 @@ class GemmPlan {
     uint32_t* ext_err_ = nullptr;
 };
 
-// Sums the split partials of EPI_PARTIAL problems in split order and applies the final
-// epilogue (bf16 / f32 / f32 += / transposed f32, alpha, residual).
-int gemm_reduce(const float* partial, int splits, int m, int n, int64_t part_stride, int epi,
-                void* out, int64_t ldo, float alpha, const uint16_t* residual, int64_t ldr,
-                int n_valid, cudaStream_t s);
-
 int num_sms();
 
-// Split count for a problem of `tiles` output tiles and `ksteps` contraction steps, chosen
-// for a fixed 148-SM machine so that the summation order never depends on the device.
-int choose_splits(int64_t tiles, int ksteps);
+// Work units of a problem: one per CTA pair = two 256-row M tiles x one N tile (>= 128 wide).
+inline int pair_tiles(int64_t m, int64_t n, int bn) {
+    const int64_t bnn = bn < kMinBN ? kMinBN : bn;
+    const int64_t mt = (m + kBM - 1) / kBM;
+    return (int)(((mt + 1) / 2) * ((n + bnn - 1) / bnn));
+}
+
+// Split count for a launch of `units` pair tiles and a problem of `ksteps` contraction steps,
+// chosen for a fixed 148-SM (74-pair) machine so that the summation order never depends on
+// the device.
+int choose_splits(int64_t units, int ksteps);
 
 struct Nf4Levels {
     float v[16];
