@@ -44,6 +44,29 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def measured_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None once the GEMM
+    kernel's sources differ from the ones the counters were taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "layer_streamed_nf4_quant_b300", "csrc")
+    for f in ("tc_gemm.cu", "tc_gemm.h", "tc_ptx.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    try:
+        lines = open(os.path.join(ROOT, "profiles", "tc_gemm_dram_traffic.md")).read().splitlines()
+    except OSError:
+        return None
+    src = next((l.split()[1] for l in lines if l.startswith("kernel_source_sha256")), None)
+    if src != h.hexdigest():
+        return None
+    for l in lines:
+        f = l.split()
+        if len(f) == 3 and f[0] == "traffic_bytes_per_launch" and f[1] == workload:
+            return int(f[2])
+    return None
+
+
 def analytic_step_flops(M, L=32, D=4096, dkv=1024, F=14336, r=64):
     """Algorithmic FLOPs of one step: forward, dX and dA/dB of every projection, no recompute."""
     shapes = [(D, D), (dkv, D), (dkv, D), (F, D), (F, D), (D, D), (D, F)]
@@ -347,7 +370,10 @@ def main(argv=None):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": "tc_gemm_kernel", "achieved": gemm_tflops, "peak": peak_tc,
                      "unit": "TFLOP/s", "frac": (gemm_tflops / peak_tc) if gemm_tflops else None,
-                     "traffic": None, "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                     "traffic": None if (args.tokens or L != 32) else measured_traffic(args.workload),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch, "
+                                       "averaged over one layer step's launches",
+                     "peak_source": f"bf16_tflops_sustained ({peak_src})",
                      "launches_per_step": prof["gemm_launches"] / args.steps,
                      "gemm_ms_per_step": prof["gemm_ms"] / args.steps},
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "bound": "h2d" if t_h2d >= t_tensor else "tensor",
