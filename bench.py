@@ -30,6 +30,10 @@ WORKLOADS = {
                                     "streamed from pinned host through two VRAM slots, batch 1 x 512 tokens"},
     "stream16k": {"M": 16384, "name": "32-layer Llama-3.1-8B-shaped NF4 + LoRA(r=64, alpha=16) stack, "
                                       "streamed from pinned host through two VRAM slots, batch 8 x 2048 tokens"},
+    "pref1024": {"M": 1024, "reference_pass": True,
+                 "name": "preference pair (chosen + rejected, 2 x 512 tokens) on the 32-layer Llama-3.1-8B-shaped "
+                         "NF4 + LoRA(r=64) stack: policy forward + backward and the adapter-disabled reference "
+                         "forward on the same streamed slots"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -67,14 +71,16 @@ def measured_traffic(workload):
     return None
 
 
-def analytic_step_flops(M, L=32, D=4096, dkv=1024, F=14336, r=64):
-    """Algorithmic FLOPs of one step: forward, dX and dA/dB of every projection, no recompute."""
+def analytic_step_flops(M, L=32, D=4096, dkv=1024, F=14336, r=64, reference_pass=False):
+    """Algorithmic FLOPs of one step: forward, dX and dA/dB of every projection, no recompute;
+    plus the adapter-disabled forward when the step runs the reference pass."""
     shapes = [(D, D), (dkv, D), (dkv, D), (F, D), (F, D), (D, D), (D, F)]
     P = sum(n * k for n, k in shapes)
     lora = sum(n + k for n, k in shapes)
     fwd = 2 * M * P + 2 * M * r * lora
     bwd = 2 * M * P + 2 * (2 * M * r * lora)   # dW-free: dY W, and dT, dB, dA, dT A
-    return L * (fwd + bwd)
+    ref = 2 * M * P if reference_pass else 0
+    return L * (fwd + bwd + ref)
 
 
 # ------------------------------------------------------------------------------ clocks
@@ -218,6 +224,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--resident", action="store_true",
                     help="read the layers from a resident device store instead of streaming them")
+    ap.add_argument("--recompute", action="store_true",
+                    help="keep only x_l per layer and recompute each layer in the reverse sweep")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -256,7 +264,9 @@ def main(argv=None):
     x0_host = x0.cpu().pin_memory()
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
-    ws = torch.empty(desc.workspace_bytes(M), dtype=torch.uint8, device=dev)
+    ref_pass = bool(wl.get("reference_pass"))
+    ws = torch.empty(desc.workspace_bytes(M, args.recompute, ref_pass), dtype=torch.uint8, device=dev)
+    x_ref = torch.empty((M, desc.d_model), dtype=torch.bfloat16, device=dev) if ref_pass else None
     slots = [torch.empty(desc.image_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
     compute = torch.cuda.Stream(device=dev)
     copy = torch.cuda.Stream(device=dev)
@@ -283,10 +293,11 @@ def main(argv=None):
     h2d_gbs = max(h2d)
 
     def step():
+        kw = dict(stream=compute, recompute=args.recompute, reference_pass=ref_pass, x_ref_out=x_ref)
         if resident is not None:
-            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, resident_store=resident, stream=compute)
+            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, resident_store=resident, **kw)
         else:
-            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, pool=pool, stream=compute)
+            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, pool=pool, **kw)
 
     for _ in range(args.warmup):
         step()
@@ -344,7 +355,8 @@ def main(argv=None):
         return 0
 
     peaks, peak_src = load_peaks()
-    step_flops = prof["gemm_flops"] / args.steps
+    exec_flops = prof["gemm_flops"] / args.steps        # executed (includes any recompute)
+    step_flops = analytic_step_flops(M, L=L, reference_pass=ref_pass)   # algorithmic
     gemm_tflops = prof["gemm_flops"] / (prof["gemm_ms"] * 1e-3) / 1e12 if prof["gemm_ms"] > 0 else None
     peak_tc = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     t_tensor = step_flops / (peak_tc * 1e12)
@@ -365,6 +377,9 @@ def main(argv=None):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl["name"], "tokens_per_step": M, "layers": L, "lora_rank": desc.rank,
+                   "recompute": bool(args.recompute), "reference_pass": ref_pass,
+                   "bytes_streamed_per_step_vs_plain_step":
+                       (pstats["bytes_copied"] / args.steps) / (2 * L * desc.image_bytes) if resident is None else 0.0,
                    "streamed_bytes_per_step": streamed_bytes, "l2": "inputs larger than L2 "
                    f"({streamed_bytes / 1e9:.2f} GB of layer images streamed per step)",
                    "parallelism": f"replicas x{world}"},
@@ -379,7 +394,7 @@ def main(argv=None):
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "bound": "h2d" if t_h2d >= t_tensor else "tensor",
                           "t_h2d_ms": t_h2d * 1e3, "t_tensor_ms": t_tensor * 1e3, "frac": t_roof / (ms * 1e-3),
                           "h2d_gbs_measured": h2d_gbs, "step_gflop": step_flops / 1e9,
-                          "step_gflop_analytic": analytic_step_flops(M, L=L) / 1e9,
+                          "step_gflop_executed": exec_flops / 1e9,
                           "copy_ms_per_step": pstats["copy_ms"] / args.steps,
                           "copy_gbs": copy_gbs},
         "cpu_baseline": cpu,

@@ -265,6 +265,36 @@ int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack
                      float* const* grads, float* loss_out, uint16_t* x_out, float* dx0,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* Options of layer_stack_step_ex (zero-initialise; NULL means all zero).
+ *
+ * recompute: checkpointed backward ([P1] "How Soup's layer streaming actually works", step 4:
+ *   under gradient checkpointing the backward recomputes the forward and so reads every
+ *   layer again).  Only x_l is kept per layer; the reverse sweep refills h, rstd, the
+ *   projections, a and the T's of each layer from its re-streamed weights before its
+ *   backward.  The workspace shrinks from about 115.6 KB to 8 KB per token per layer (plus
+ *   one layer's set); results are bit-identical to the stored-activation run.
+ * reference_pass: preference-pair reuse ([P4] "In detail": the DPO reference model is the
+ *   same base stream with the adapter disabled).  In the forward sweep each layer also runs
+ *   the frozen base alone (the LoRA contraction steps are left out, not multiplied by zero)
+ *   on its own residual stream from x0, against the same streamed slot before it is
+ *   released, so no layer is copied more often than without it.  The backward and the loss
+ *   concern the policy (adapter) branch only; x_ref_out receives the reference output. */
+typedef struct {
+    int32_t recompute;
+    int32_t reference_pass;
+    int32_t reserved[6];
+} lsn_step_opts;
+
+size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts* opts);
+
+/* layer_stack_step with options.  x_ref_out (nullable, device bf16 [M x d_model]) receives
+ * the reference-pass output when opts->reference_pass is set. */
+int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_stack_desc* desc,
+                        const lsn_step_opts* opts, const uint16_t* x0, int64_t M,
+                        const uint16_t* const* lora, float* const* grads, float* loss_out,
+                        uint16_t* x_out, uint16_t* x_ref_out, float* dx0, void* ws, size_t ws_bytes,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

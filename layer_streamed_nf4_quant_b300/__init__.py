@@ -13,7 +13,7 @@ import ctypes as C
 import numpy as np
 
 from ._lib import (LSN_ECORRUPT, LSN_EINVAL, LSN_ENOMEM, LSN_ESTATE, LSN_ETIMEOUT, LSN_OK,  # noqa: F401
-                   LsnError, check, lib, lsn_pool_stats, lsn_profile, lsn_stack_desc, nf4_view)
+                   LsnError, check, lib, lsn_pool_stats, lsn_profile, lsn_stack_desc, lsn_step_opts, nf4_view)
 
 PROJ = ("q", "k", "v", "gate", "up", "o", "down")   # canonical projection order
 
@@ -235,8 +235,11 @@ class StackDesc:
         return {"q": (D, D), "k": (dkv, D), "v": (dkv, D), "gate": (F, D), "up": (F, D), "o": (D, D),
                 "down": (D, F)}[p]
 
-    def workspace_bytes(self, M: int) -> int:
-        return int(lib.lsn_stack_workspace_bytes(C.byref(self.c), M))
+    def workspace_bytes(self, M: int, recompute: bool = False, reference_pass: bool = False) -> int:
+        if not (recompute or reference_pass):
+            return int(lib.lsn_stack_workspace_bytes(C.byref(self.c), M))
+        o = lsn_step_opts(1 if recompute else 0, 1 if reference_pass else 0)
+        return int(lib.lsn_stack_workspace_bytes_ex(C.byref(self.c), M, C.byref(o)))
 
     def pack_layer(self, layer: int, W: dict, dst: np.ndarray | None = None, n_threads: int = 0) -> np.ndarray:
         """Packs one layer image (header + seven NF4 matrices) from fp32 numpy weights."""
@@ -263,11 +266,22 @@ class StackDesc:
 
 
 def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
-                     resident_store=None, x_out=None, dx0=None, stream=None):
-    """One forward + loss + backward pass over the stack (streamed through `pool`, or resident)."""
+                     resident_store=None, x_out=None, dx0=None, stream=None, recompute: bool = False,
+                     reference_pass: bool = False, x_ref_out=None):
+    """One forward + loss + backward pass over the stack (streamed through `pool`, or resident).
+
+    recompute: keep only x_l per layer and recompute the rest in the reverse sweep.
+    reference_pass: also run the adapter-disabled forward on the same streamed slots and write
+    it to x_ref_out."""
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
-    check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
-                               _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws), ws.numel(),
-                               _stream(stream)))
+    if not (recompute or reference_pass or x_ref_out is not None):
+        check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
+                                   _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws),
+                                   ws.numel(), _stream(stream)))
+        return
+    o = lsn_step_opts(1 if recompute else 0, 1 if reference_pass else 0)
+    check(lib.layer_stack_step_ex(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
+                                  C.byref(o), _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(x_ref_out),
+                                  _p(dx0), _p(ws), ws.numel(), _stream(stream)))

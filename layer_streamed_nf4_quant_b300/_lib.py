@@ -40,6 +40,10 @@ class lsn_stack_desc(C.Structure):
                 ("rms_eps", C.c_float), ("kv_loss_coef", C.c_float)]
 
 
+class lsn_step_opts(C.Structure):
+    _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6)]
+
+
 class lsn_profile(C.Structure):
     _fields_ = [("gemm_launches", C.c_uint64), ("gemm_ms", C.c_double), ("gemm_flops", C.c_double)]
 
@@ -83,6 +87,9 @@ SIGNATURES = {
     "lsn_stack_workspace_bytes": (SZ, [C.POINTER(lsn_stack_desc), I64]),
     "layer_stack_step": (I, [P, P, C.POINTER(lsn_stack_desc), P, I64, C.POINTER(P), C.POINTER(P), P, P, P,
                              P, SZ, P]),
+    "lsn_stack_workspace_bytes_ex": (SZ, [C.POINTER(lsn_stack_desc), I64, C.POINTER(lsn_step_opts)]),
+    "layer_stack_step_ex": (I, [P, P, C.POINTER(lsn_stack_desc), C.POINTER(lsn_step_opts), P, I64, C.POINTER(P),
+                                C.POINTER(P), P, P, P, P, P, SZ, P]),
 }
 
 

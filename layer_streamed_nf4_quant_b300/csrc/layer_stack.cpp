@@ -57,6 +57,12 @@ struct Buffers {
     float* xpart = nullptr;
     float* partial = nullptr;
     size_t partial_bytes = 0;
+    // reference (adapter disabled) pass: residual stream ping-pong and per-layer scratch
+    uint16_t* xr[2] = {nullptr, nullptr};
+    uint16_t* hr = nullptr;
+    float* rstdr = nullptr;
+    uint16_t* yr = nullptr;
+    uint16_t* ar = nullptr;
 };
 
 bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
@@ -89,7 +95,10 @@ bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
 }
 
 // Lays the activations and scratch out in ws (base == nullptr: only sizes).  Returns bytes.
-size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size_t partial_bytes) {
+// With recompute, only x_l is kept per layer; h, rstd, the projections, a and the T's live in
+// one set of buffers that the reverse sweep refills by recomputing the layer.
+size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size_t partial_bytes,
+              const lsn_step_opts& o) {
     size_t off = 0;
     auto take = [&](size_t bytes) -> uint8_t* {
         uint8_t* p = base ? base + off : nullptr;
@@ -107,6 +116,15 @@ size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size
     b->x[0] = const_cast<uint16_t*>(x0);
     for (int l = 0; l < d.L; ++l) {
         b->x[l + 1] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        if (o.recompute && l > 0) {
+            b->h[l] = b->h[0];
+            b->rstd[l] = b->rstd[0];
+            b->y[l] = b->y[0];
+            b->a[l] = b->a[0];
+            b->tcat[l] = b->tcat[0];
+            b->tod[l] = b->tod[0];
+            continue;
+        }
         b->h[l] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
         b->rstd[l] = reinterpret_cast<float*>(take(M * 4));
         b->y[l] = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
@@ -123,6 +141,14 @@ size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size
     b->dh = reinterpret_cast<float*>(take(M * d.D * 4));
     b->kvpart = reinterpret_cast<float*>(take((size_t)d.L * kLossBlocks * 2 * 4));
     b->xpart = reinterpret_cast<float*>(take((size_t)kLossBlocks * 4));
+    if (o.reference_pass) {
+        b->xr[0] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        b->xr[1] = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        b->hr = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
+        b->rstdr = reinterpret_cast<float*>(take(M * 4));
+        b->yr = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
+        b->ar = reinterpret_cast<uint16_t*>(take(M * d.F * 2));
+    }
     b->partial = reinterpret_cast<float*>(take(partial_bytes));
     b->partial_bytes = partial_bytes;
     return off;
@@ -131,6 +157,7 @@ size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size
 struct Ctx {
     Dims d;
     Buffers b;
+    lsn_step_opts o{};
     cudaStream_t s = nullptr;
     bool dry = false;
     size_t partial_need = 0;
@@ -160,7 +187,9 @@ struct Ctx {
 
 // --------------------------------------------------------------------------- forward
 
-int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora) {
+// recompute: the reverse sweep's refill of this layer's stored activations (the output x'
+// and the loss terms are already known, so the O+down GEMM and the k/v sums are skipped).
+int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool recompute = false) {
     const Dims& d = c.d;
     const Buffers& b = c.b;
     const int M = d.M, D = d.D, r = d.r;
@@ -205,6 +234,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora) {
         g.seg(ma, 0, B_TMA_K, mad, 0, 0, d.F);
         RC(c.run(g));
     }
+    if (recompute) return LSN_OK;
     {   // x' = bf16(x + q W_o^T + a W_d^T + s T_o B_o^T + s T_d B_d^T)
         GemmPlan g(c.dry);
         int mq = g.map(b.y[l], M, D, d.Ncat, kBM);
@@ -222,6 +252,45 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora) {
     }
     if (!c.dry)
         RC(launch_kv_sumsq(b.y[l], d.Ncat, d.coff[1], d.coff[2], d.dkv, M, b.kvpart + (size_t)l * kLossBlocks * 2, c.s));
+    return LSN_OK;
+}
+
+// ------------------------------------------------------- reference (adapter disabled)
+
+// The frozen base alone on the same streamed weights: the LoRA contraction steps are left
+// out of the GEMMs (not multiplied by zero).  xin -> xout, scratch shared by all layers.
+int ref_layer(Ctx& c, const uint8_t* img, const uint16_t* xin, uint16_t* xout) {
+    const Dims& d = c.d;
+    const Buffers& b = c.b;
+    const int M = d.M, D = d.D;
+    if (!c.dry) RC(launch_rmsnorm_fwd(xin, b.hr, b.rstdr, M, D, d.eps, nullptr, 0, c.s));
+    {
+        GemmPlan g(c.dry);
+        int mh = g.map(b.hr, M, D, D, kBM);
+        int tiles = 0;
+        for (int p = 0; p < 5; ++p) tiles += tiles_of(M, d.np[p], 256);
+        const int sp = choose_splits(tiles, D / kBK);
+        for (int p = 0; p < 5; ++p) {
+            int v = g.nf4(c.mat(img, p), d.np[p], D);
+            g.problem(M, d.np[p], 256, A_KMAJOR, EPI_BF16, b.yr ? b.yr + d.coff[p] : nullptr, d.Ncat, 1.0f, d.np[p],
+                      sp);
+            g.seg(mh, 0, B_NF4_K, v, 0, 0, D);
+        }
+        RC(c.run(g));
+    }
+    if (!c.dry) RC(launch_silu_mul(b.yr, d.Ncat, d.coff[3], d.coff[4], b.ar, M, d.F, c.s));
+    {
+        GemmPlan g(c.dry);
+        int mq = g.map(b.yr, M, D, d.Ncat, kBM);
+        int ma = g.map(b.ar, M, d.F, d.F, kBM);
+        int vo = g.nf4(c.mat(img, kO), D, D);
+        int vd = g.nf4(c.mat(img, kDown), D, d.F);
+        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, xout, D, 1.0f, D,
+                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK), xin, D);
+        g.seg(mq, 0, B_NF4_K, vo, 0, 0, D);
+        g.seg(ma, 0, B_NF4_K, vd, 0, 0, d.F);
+        RC(c.run(g));
+    }
     return LSN_OK;
 }
 
@@ -337,31 +406,45 @@ int init_ctx(Ctx& c, const lsn_stack_desc* desc, int64_t M) {
     return LSN_OK;
 }
 
-size_t partial_need(const lsn_stack_desc* desc, int64_t M) {
+size_t partial_need(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts& o) {
     Ctx c;
     if (init_ctx(c, desc, M)) return 0;
     c.dry = true;
-    layout(c.d, nullptr, nullptr, &c.b, 0);
+    c.o = o;
+    layout(c.d, nullptr, nullptr, &c.b, 0, o);
     if (fwd_layer(c, 0, nullptr, nullptr) || bwd_layer(c, 0, nullptr, nullptr, nullptr)) return 0;
+    if (o.reference_pass && ref_layer(c, nullptr, nullptr, nullptr)) return 0;
     return c.partial_need;
+}
+
+lsn_step_opts opts_or_default(const lsn_step_opts* o) {
+    lsn_step_opts d{};
+    return o ? *o : d;
 }
 
 }  // namespace
 
 extern "C" {
 
-size_t lsn_stack_workspace_bytes(const lsn_stack_desc* desc, int64_t M) {
+size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts* opts) {
     Ctx c;
     if (init_ctx(c, desc, M)) return 0;
+    const lsn_step_opts o = opts_or_default(opts);
     Buffers b;
-    return layout(c.d, nullptr, nullptr, &b, partial_need(desc, M)) + 256;
+    return layout(c.d, nullptr, nullptr, &b, partial_need(desc, M, o), o) + 256;
 }
 
-int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack_desc* desc, const uint16_t* x0,
-                     int64_t M, const uint16_t* const* lora, float* const* grads, float* loss_out, uint16_t* x_out,
-                     float* dx0, void* ws, size_t ws_bytes, void* stream) {
+size_t lsn_stack_workspace_bytes(const lsn_stack_desc* desc, int64_t M) {
+    return lsn_stack_workspace_bytes_ex(desc, M, nullptr);
+}
+
+int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_stack_desc* desc,
+                        const lsn_step_opts* opts, const uint16_t* x0, int64_t M, const uint16_t* const* lora,
+                        float* const* grads, float* loss_out, uint16_t* x_out, uint16_t* x_ref_out, float* dx0,
+                        void* ws, size_t ws_bytes, void* stream) {
     Ctx c;
     RC(init_ctx(c, desc, M));
+    c.o = opts_or_default(opts);
     if (!x0 || !lora || !grads || !loss_out || !ws || (!pool && !resident_store))
         return fail(LSN_EINVAL, "layer_stack_step: NULL argument");
     if ((reinterpret_cast<uintptr_t>(ws) & 255) || (reinterpret_cast<uintptr_t>(x0) & 15))
@@ -370,10 +453,10 @@ int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack
         if (!lora[l] || !grads[l] || (reinterpret_cast<uintptr_t>(lora[l]) & 15) ||
             (reinterpret_cast<uintptr_t>(grads[l]) & 15))
             return fail(LSN_EINVAL, "layer_stack_step: LoRA / grad blob %d missing or misaligned", l);
-    const size_t pneed = partial_need(desc, M);
-    const size_t need = layout(c.d, nullptr, nullptr, &c.b, pneed);
+    const size_t pneed = partial_need(desc, M, c.o);
+    const size_t need = layout(c.d, nullptr, nullptr, &c.b, pneed, c.o);
     if (ws_bytes < need) return fail(LSN_ENOMEM, "layer_stack_step: workspace %zu < %zu", ws_bytes, need);
-    layout(c.d, static_cast<uint8_t*>(ws), x0, &c.b, pneed);
+    layout(c.d, static_cast<uint8_t*>(ws), x0, &c.b, pneed, c.o);
     c.s = static_cast<cudaStream_t>(stream);
     const size_t img_bytes = lsn_layer_image_bytes(desc);
     const uint8_t* res = static_cast<const uint8_t*>(resident_store);
@@ -389,30 +472,47 @@ int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack
         return rc;
     };
 
-    // forward sweep, prefetching one layer ahead
+    // forward sweep, prefetching one layer ahead; the reference pass (if any) runs on the
+    // same slot before it is released, so it costs no extra copy
     if (pool) RC(stream_pool_prefetch(pool, 0));
+    const uint16_t* xr_in = x0;
     for (int l = 0; l < L; ++l) {
         if (pool && l + 1 < L) RC(stream_pool_prefetch(pool, l + 1));
         const uint8_t* img;
         RC(image(l, &img));
         RC(fwd_layer(c, l, img, lora[l]));
+        if (c.o.reference_pass) {
+            uint16_t* xr_out = c.b.xr[l & 1];
+            RC(ref_layer(c, img, xr_in, xr_out));
+            xr_in = xr_out;
+        }
         if (pool) RC(stream_pool_release(pool, l, stream));
     }
     RC(launch_loss(c.b.x[L], c.d.M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart, loss_out,
                    c.s));
-    // reverse sweep, re-streaming every layer
+    // reverse sweep, re-streaming every layer (and recomputing its activations if asked)
     if (pool) RC(stream_pool_prefetch(pool, L - 1));
     for (int l = L - 1; l >= 0; --l) {
         if (pool && l - 1 >= 0) RC(stream_pool_prefetch(pool, l - 1));
         const uint8_t* img;
         RC(image(l, &img));
+        if (c.o.recompute) RC(fwd_layer(c, l, img, lora[l], true));
         RC(bwd_layer(c, l, img, lora[l], grads[l]));
         if (pool) RC(stream_pool_release(pool, l, stream));
     }
     if (x_out)
         LSN_CUDA_TRY(cudaMemcpyAsync(x_out, c.b.x[L], (size_t)c.d.M * c.d.D * 2, cudaMemcpyDeviceToDevice, c.s));
+    if (x_ref_out && c.o.reference_pass)
+        LSN_CUDA_TRY(cudaMemcpyAsync(x_ref_out, xr_in, (size_t)c.d.M * c.d.D * 2, cudaMemcpyDeviceToDevice, c.s));
     if (dx0) LSN_CUDA_TRY(cudaMemcpyAsync(dx0, c.b.dx, (size_t)c.d.M * c.d.D * 4, cudaMemcpyDeviceToDevice, c.s));
     return LSN_OK;
+}
+
+int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack_desc* desc, const uint16_t* x0,
+                     int64_t M, const uint16_t* const* lora, float* const* grads, float* loss_out, uint16_t* x_out,
+                     float* dx0, void* ws, size_t ws_bytes, void* stream) {
+    return layer_stack_step_ex(pool, resident_store, desc, nullptr, x0, M, lora, grads, loss_out, x_out, nullptr, dx0,
+                               ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -135,3 +135,20 @@ def stack_forward_backward(x0, layers, scale, eps=1e-5, kv_coef=1e-3, rnd=True,
         dx, dAs[li], dBs[li] = layer_backward(c, dx, W, A, B, scale, coef * c["k"], coef * c["v"])
     return {"loss": loss, "x_last": xs[-1], "xs": xs, "caches": caches,
             "dA": dAs, "dB": dBs, "dx0": dx}
+
+
+def frozen_stack_forward(x0, Ws, eps=1e-5, rnd=True):
+    """The reference model of preference training: the same frozen base with the adapter
+    disabled (the rug.gal radar item "soup-fine-tune-8b-4gb-laptop-gpu-layer-streaming",
+    section "In detail": the DPO reference model reuses the base stream without LoRA).
+    Ws: list of per-layer weight dicts.  Each layer is the synthetic layer with no LoRA terms:
+    h = rmsnorm(x); p = h W_p^T; a = silu(gate) up; x' = x + q W_o^T + a W_d^T."""
+    R = bf16_round if rnd else (lambda t: np.asarray(t, np.float64))
+    x = np.asarray(x0, np.float64)
+    for W in Ws:
+        h, _ = rmsnorm_forward(x, eps)
+        h = R(h)
+        out = {p: R(h @ np.asarray(W[p], np.float64).T) for p in QKVGU}
+        a = R(silu(out["gate"]) * out["up"])
+        x = R(x + out["q"] @ np.asarray(W["o"], np.float64).T + a @ np.asarray(W["down"], np.float64).T)
+    return x

@@ -93,3 +93,13 @@ def test_layer_image_pack_small():
         n, k = d.shape(p)
         want = np.frombuffer(onf4.pack(onf4.quantize(W[p])), np.uint8)
         np.testing.assert_array_equal(img[d.image_offsets[i]: d.image_offsets[i] + want.nbytes], want)
+
+
+def test_recompute_workspace_is_smaller():
+    d = lsn.StackDesc()
+    full = d.workspace_bytes(16384)
+    rec = d.workspace_bytes(16384, recompute=True)
+    ref = d.workspace_bytes(512, reference_pass=True)
+    assert rec < full / 5                      # only x_l (8 KB per token) is kept per layer
+    assert full > 32 * 16384 * 115_000          # all activations of 32 layers at 16K tokens
+    assert ref > d.workspace_bytes(512)

@@ -42,7 +42,7 @@ class Stack:
         return lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
                               self.copy_stream, first_slot=first_slot, reuse_resident=reuse)
 
-    def run(self, pool=None):
+    def run(self, pool=None, recompute=False, reference=False):
         lsn = _lsn()
         d = self.desc
         grads = [torch.full((d.lora_elems,), float("nan"), dtype=torch.float32, device="cuda")
@@ -50,11 +50,16 @@ class Stack:
         loss = torch.zeros(1, dtype=torch.float32, device="cuda")
         x_out = torch.empty((self.M, d.d_model), dtype=torch.bfloat16, device="cuda")
         dx0 = torch.empty((self.M, d.d_model), dtype=torch.float32, device="cuda")
-        lsn.layer_stack_step(d, self.x0, self.lora, grads, loss, self.ws, pool=pool,
-                             resident_store=None if pool else self.resident, x_out=x_out, dx0=dx0)
+        x_ref = torch.empty((self.M, d.d_model), dtype=torch.bfloat16, device="cuda") if reference else None
+        ws = self.ws
+        if recompute or reference:
+            ws = torch.empty(d.workspace_bytes(self.M, recompute, reference), dtype=torch.uint8, device="cuda")
+        lsn.layer_stack_step(d, self.x0, self.lora, grads, loss, ws, pool=pool,
+                             resident_store=None if pool else self.resident, x_out=x_out, dx0=dx0,
+                             recompute=recompute, reference_pass=reference, x_ref_out=x_ref)
         torch.cuda.synchronize()
         assert lsn.device_check() == 0
-        return {"loss": loss, "x": x_out, "dx0": dx0, "grads": grads}
+        return {"loss": loss, "x": x_out, "dx0": dx0, "grads": grads, "x_ref": x_ref}
 
 
 def _same(a, b):
@@ -138,6 +143,45 @@ def test_small_replay_slot_parity_and_delays(small):
     _same(base, small.run(pool))
     assert pool.stats()["skipped"] == 2
     pool.close()
+
+
+def test_recompute_bit_identical_to_stored_activations(small):
+    """The checkpointed backward (only x_l kept, each layer recomputed from its re-streamed
+    weights) gives the stored-activation run's bits, resident and streamed."""
+    base = small.run()
+    _same(base, small.run(recompute=True))
+    pool = small.pool()
+    _same(base, small.run(pool, recompute=True))
+    assert pool.stats()["copies"] == 2 * small.desc.n_layers
+    pool.close()
+
+
+def test_reference_pass_shares_the_stream(small):
+    """Preference-pair reuse: the adapter-disabled forward runs on the same streamed slots.
+    It matches the oracle's frozen-base forward, leaves the policy branch's bits unchanged,
+    and copies no layer more often than the plain step (bytes streamed per step x1.0)."""
+    from oracle import nf4 as onf4
+    from oracle import stack as ostack
+    from oracle.nf4 import bf16_value
+    import synth
+    base = small.run()
+    pool = small.pool()
+    out = small.run(pool, reference=True)
+    _same(base, out)
+    stats = pool.stats()
+    assert stats["copies"] == 2 * small.desc.n_layers
+    assert stats["bytes_copied"] == 2 * small.desc.n_layers * small.desc.image_bytes
+    pool.close()
+    d = small.desc
+    Ws = []
+    for l in range(d.n_layers):
+        W = synth.layer_weights(l, d.d_model, d.d_kv, d.d_ff)
+        Ws.append({p: onf4.dequantize(onf4.quantize(W[p])) for p in W})
+    ref = ostack.frozen_stack_forward(bf16_value(small.x0_bits).astype(np.float64), Ws)
+    got = bf16_value(_bits(out["x_ref"])).astype(np.float64)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= FWD_TOL
+    x_pol = bf16_value(_bits(out["x"])).astype(np.float64)
+    assert np.max(np.abs(got - x_pol)) > 0                   # the adapter does change the output
 
 
 def test_pool_misuse_is_reported(small):

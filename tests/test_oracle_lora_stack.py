@@ -160,3 +160,24 @@ def test_rounded_path_close_to_unrounded():
         for p in PROJ:
             num = np.linalg.norm(a["dA"][li][p] - b["dA"][li][p])
             assert num / np.linalg.norm(a["dA"][li][p]) < 5e-2
+
+
+def test_frozen_forward_closed_forms():
+    """Zero weights make every layer the identity; with weights it equals the policy forward
+    whose adapter outputs are zero (B = 0), and differs once B is non-zero."""
+    rng = np.random.default_rng(30)
+    d, dkv, dff, r = 32, 16, 48, 4
+    layers = _tiny_layers(rng, 2, d, dkv, dff, r)
+    x0 = _rand(rng, 5, d)
+    zeros = [{p: np.zeros_like(W[p]) for p in W} for (W, _, _) in layers]
+    np.testing.assert_array_equal(stack.frozen_stack_forward(x0, zeros, rnd=False), x0)
+    ref = stack.frozen_stack_forward(x0, [W for (W, _, _) in layers], rnd=False)
+    no_adapter = [(W, A, {p: np.zeros_like(B[p]) for p in B}) for (W, A, B) in layers]
+    x = x0
+    for (W, A, B) in no_adapter:
+        x, _ = stack.layer_forward(x, W, A, B, 0.25, rnd=False)
+    np.testing.assert_allclose(ref, x, rtol=1e-13, atol=1e-13)
+    x = x0
+    for (W, A, B) in layers:
+        x, _ = stack.layer_forward(x, W, A, B, 0.25, rnd=False)
+    assert np.max(np.abs(ref - x)) > 1e-6
