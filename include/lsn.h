@@ -279,13 +279,42 @@ int layer_stack_step(lsn_pool* pool, const void* resident_store, const lsn_stack
  *   on its own residual stream from x0, against the same streamed slot before it is
  *   released, so no layer is copied more often than without it.  The backward and the loss
  *   concern the policy (adapter) branch only; x_ref_out receives the reference output. */
+/* AdamW hyper-parameters (decoupled weight decay); step = t >= 1 sets the bias corrections. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int32_t step;
+} lsn_adamw_hparams;
+
+/* Optimizer state for the fused update of layer_stack_step_ex: per layer, device fp32
+ * arrays of lsn_lora_elems() (master copy, first and second moment) and the bf16 LoRA blob
+ * that receives bf16(master) after the update (normally the blob the step reads). */
+typedef struct {
+    lsn_adamw_hparams hp;
+    float* const* master;
+    float* const* m;
+    float* const* v;
+    uint16_t* const* lora_out;
+} lsn_adamw_state;
+
 typedef struct {
     int32_t recompute;
     int32_t reference_pass;
     int32_t reserved[6];
+    /* nullable: when set, each layer's AdamW update runs in the reverse sweep right after
+     * that layer's dA/dB are written (they are still written to grads). */
+    const lsn_adamw_state* adamw;
 } lsn_step_opts;
 
 size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts* opts);
+
+/* One AdamW step over n parameters (the pages set lr 2e-5 in "Fine tune an 8B model on a
+ * 4GB laptop GPU (Soup setup)", "Step 1, the config"; they name no optimizer):
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p = p - lr ((m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps) + wd p)
+ * p, m, v: device fp32 [n] (updated in place); g: device fp32 [n]; p_bf16 (nullable): device
+ * bf16 [n] receives bf16(p).  All pointers 16-byte aligned.  Elementwise, in fp32. */
+int lsn_adamw_step(const lsn_adamw_hparams* hp, float* p, uint16_t* p_bf16, const float* g, float* m,
+                   float* v, size_t n, void* stream);
 
 /* layer_stack_step with options.  x_ref_out (nullable, device bf16 [M x d_model]) receives
  * the reference-pass output when opts->reference_pass is set. */

@@ -13,7 +13,8 @@ import ctypes as C
 import numpy as np
 
 from ._lib import (LSN_ECORRUPT, LSN_EINVAL, LSN_ENOMEM, LSN_ESTATE, LSN_ETIMEOUT, LSN_OK,  # noqa: F401
-                   LsnError, check, lib, lsn_pool_stats, lsn_profile, lsn_stack_desc, lsn_step_opts, nf4_view)
+                   LsnError, check, lib, lsn_adamw_hparams, lsn_adamw_state, lsn_pool_stats, lsn_profile,
+                   lsn_stack_desc, lsn_step_opts, nf4_view)
 
 PROJ = ("q", "k", "v", "gate", "up", "o", "down")   # canonical projection order
 
@@ -133,6 +134,14 @@ def lora_nf4_bwd(packed, n_out, k_in, X, T, dY, A, B, r, scale, dX=None, accumul
                            _p(dX if want_dX else None), 1 if accumulate_dX else 0, _p(dA), _p(dB), _p(ws),
                            ws.numel(), _stream(stream)))
     return dX, dA, dB
+
+
+def adamw_step(p, g, m, v, step: int, lr: float, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, p_bf16=None,
+               stream=None):
+    """One AdamW step on fp32 device tensors p, m, v (in place) with gradient g; writes
+    bf16(p) into p_bf16 when given."""
+    hp = lsn_adamw_hparams(lr, beta1, beta2, eps, weight_decay, step)
+    check(lib.lsn_adamw_step(C.byref(hp), _p(p), _p(p_bf16), _p(g), _p(m), _p(v), p.numel(), _stream(stream)))
 
 
 def device_check(stream=None) -> int:
@@ -265,9 +274,30 @@ class StackDesc:
         return A, B
 
 
+class AdamW:
+    """Per-layer AdamW state for the update fused into the reverse sweep: fp32 master copies
+    (initialised from the bf16 LoRA blobs), zero moments, and the blobs it refreshes."""
+
+    def __init__(self, lora_blobs, lr=2e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0):
+        torch = _torch()
+        self.blobs = lora_blobs
+        self.master = [b.float().clone() for b in lora_blobs]
+        self.m = [torch.zeros_like(x) for x in self.master]
+        self.v = [torch.zeros_like(x) for x in self.master]
+        self.hp = lsn_adamw_hparams(lr, beta1, beta2, eps, weight_decay, 0)
+
+    def state(self):
+        """The C struct for the next step (advances the step counter)."""
+        self.hp.step += 1
+        L = len(self.blobs)
+        self._arrays = [(C.c_void_p * L)(*[t.data_ptr() for t in ts])
+                        for ts in (self.master, self.m, self.v, self.blobs)]
+        return lsn_adamw_state(self.hp, *self._arrays)
+
+
 def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
                      resident_store=None, x_out=None, dx0=None, stream=None, recompute: bool = False,
-                     reference_pass: bool = False, x_ref_out=None):
+                     reference_pass: bool = False, x_ref_out=None, adamw: "AdamW | None" = None):
     """One forward + loss + backward pass over the stack (streamed through `pool`, or resident).
 
     recompute: keep only x_l per layer and recompute the rest in the reverse sweep.
@@ -276,12 +306,15 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
-    if not (recompute or reference_pass or x_ref_out is not None):
+    if not (recompute or reference_pass or x_ref_out is not None or adamw is not None):
         check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                    _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws),
                                    ws.numel(), _stream(stream)))
         return
     o = lsn_step_opts(1 if recompute else 0, 1 if reference_pass else 0)
+    if adamw is not None:
+        st = adamw.state()
+        o.adamw = C.pointer(st)
     check(lib.layer_stack_step_ex(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                   C.byref(o), _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(x_ref_out),
                                   _p(dx0), _p(ws), ws.numel(), _stream(stream)))

@@ -40,8 +40,19 @@ class lsn_stack_desc(C.Structure):
                 ("rms_eps", C.c_float), ("kv_loss_coef", C.c_float)]
 
 
+class lsn_adamw_hparams(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
+                ("weight_decay", C.c_float), ("step", C.c_int32)]
+
+
+class lsn_adamw_state(C.Structure):
+    _fields_ = [("hp", lsn_adamw_hparams), ("master", C.POINTER(C.c_void_p)), ("m", C.POINTER(C.c_void_p)),
+                ("v", C.POINTER(C.c_void_p)), ("lora_out", C.POINTER(C.c_void_p))]
+
+
 class lsn_step_opts(C.Structure):
-    _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6)]
+    _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6),
+                ("adamw", C.POINTER(lsn_adamw_state))]
 
 
 class lsn_profile(C.Structure):
@@ -88,6 +99,7 @@ SIGNATURES = {
     "layer_stack_step": (I, [P, P, C.POINTER(lsn_stack_desc), P, I64, C.POINTER(P), C.POINTER(P), P, P, P,
                              P, SZ, P]),
     "lsn_stack_workspace_bytes_ex": (SZ, [C.POINTER(lsn_stack_desc), I64, C.POINTER(lsn_step_opts)]),
+    "lsn_adamw_step": (I, [C.POINTER(lsn_adamw_hparams), P, P, P, P, P, SZ, P]),
     "layer_stack_step_ex": (I, [P, P, C.POINTER(lsn_stack_desc), C.POINTER(lsn_step_opts), P, I64, C.POINTER(P),
                                 C.POINTER(P), P, P, P, P, P, SZ, P]),
 }

@@ -293,6 +293,31 @@ __global__ void dy_build_kernel(const float* __restrict__ dqa, const uint16_t* _
     }
 }
 
+// -------------------------------------------------------------------------- AdamW
+
+__global__ void adamw_kernel(float* __restrict__ p, uint16_t* __restrict__ pb, const float* __restrict__ g,
+                             float* __restrict__ m, float* __restrict__ v, int64_t n, float lr, float b1, float b2,
+                             float eps, float wd, float bc1, float bc2) {
+    const float omb1 = 1.0f - b1, omb2 = 1.0f - b2;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float gi = g[i];
+        const float mi = __fadd_rn(__fmul_rn(b1, m[i]), __fmul_rn(omb1, gi));
+        const float vi = __fadd_rn(__fmul_rn(b2, v[i]), __fmul_rn(omb2, __fmul_rn(gi, gi)));
+        const float mh = __fdiv_rn(mi, bc1);
+        const float vh = __fdiv_rn(vi, bc2);
+        const float pi = p[i];
+        const float upd = __fadd_rn(__fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), eps)), __fmul_rn(wd, pi));
+        const float pn = __fsub_rn(pi, __fmul_rn(lr, upd));
+        m[i] = mi;
+        v[i] = vi;
+        p[i] = pn;
+        if (pb) {
+            __nv_bfloat16 h = __float2bfloat16_rn(pn);
+            pb[i] = *reinterpret_cast<uint16_t*>(&h);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------- launchers
 
 static inline unsigned grid_for(int64_t work, int per_block) {
@@ -366,4 +391,24 @@ int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, in
     return LSN_OK;
 }
 
+int launch_adamw(const lsn_adamw_hparams& hp, float* p, uint16_t* pb, const float* g, float* m, float* v, int64_t n,
+                 cudaStream_t s) {
+    const double bc1 = 1.0 - pow((double)hp.beta1, (double)hp.step);
+    const double bc2 = 1.0 - pow((double)hp.beta2, (double)hp.step);
+    adamw_kernel<<<grid_for(n, 256), 256, 0, s>>>(p, pb, g, m, v, n, hp.lr, hp.beta1, hp.beta2, hp.eps,
+                                                  hp.weight_decay, (float)bc1, (float)bc2);
+    note_launch();
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
 }  // namespace lsn
+
+extern "C" int lsn_adamw_step(const lsn_adamw_hparams* hp, float* p, uint16_t* p_bf16, const float* g, float* m,
+                              float* v, size_t n, void* stream) {
+    using namespace lsn;
+    if (!hp || !p || !g || !m || !v || n == 0) return fail(LSN_EINVAL, "lsn_adamw_step: bad arguments");
+    if (hp->step < 1 || !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f))
+        return fail(LSN_EINVAL, "lsn_adamw_step: need step >= 1 and betas in [0, 1)");
+    return launch_adamw(*hp, p, p_bf16, g, m, v, (int64_t)n, static_cast<cudaStream_t>(stream));
+}

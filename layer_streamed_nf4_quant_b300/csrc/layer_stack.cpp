@@ -453,6 +453,14 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         if (!lora[l] || !grads[l] || (reinterpret_cast<uintptr_t>(lora[l]) & 15) ||
             (reinterpret_cast<uintptr_t>(grads[l]) & 15))
             return fail(LSN_EINVAL, "layer_stack_step: LoRA / grad blob %d missing or misaligned", l);
+    if (c.o.adamw) {
+        const lsn_adamw_state* st = c.o.adamw;
+        if (!st->master || !st->m || !st->v || !st->lora_out || st->hp.step < 1)
+            return fail(LSN_EINVAL, "layer_stack_step: incomplete AdamW state");
+        for (int l = 0; l < c.d.L; ++l)
+            if (!st->master[l] || !st->m[l] || !st->v[l] || !st->lora_out[l])
+                return fail(LSN_EINVAL, "layer_stack_step: AdamW state of layer %d missing", l);
+    }
     const size_t pneed = partial_need(desc, M, c.o);
     const size_t need = layout(c.d, nullptr, nullptr, &c.b, pneed, c.o);
     if (ws_bytes < need) return fail(LSN_ENOMEM, "layer_stack_step: workspace %zu < %zu", ws_bytes, need);
@@ -498,6 +506,11 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         RC(image(l, &img));
         if (c.o.recompute) RC(fwd_layer(c, l, img, lora[l], true));
         RC(bwd_layer(c, l, img, lora[l], grads[l]));
+        if (c.o.adamw) {
+            const lsn_adamw_state* st = c.o.adamw;
+            RC(launch_adamw(st->hp, st->master[l], st->lora_out[l], grads[l], st->m[l], st->v[l],
+                            (int64_t)lsn_lora_elems(desc), c.s));
+        }
         if (pool) RC(stream_pool_release(pool, l, stream));
     }
     if (x_out)

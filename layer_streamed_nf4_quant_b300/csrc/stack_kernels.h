@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "lsn.h"
+
 namespace lsn {
 
 constexpr int kLossBlocks = 128;   // fixed grid of the loss reductions (fixes their order)
@@ -27,5 +29,9 @@ int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv
 // dY_cat = [dq | 2c k/(M dkv) | 2c v/(M dkv) | dgate | dup] in bf16.
 int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
                     float kv_coef, cudaStream_t s);
+
+// One AdamW step over n fp32 parameters (bf16 copy into pb when non-null).
+int launch_adamw(const lsn_adamw_hparams& hp, float* p, uint16_t* pb, const float* g, float* m, float* v, int64_t n,
+                 cudaStream_t s);
 
 }  // namespace lsn
