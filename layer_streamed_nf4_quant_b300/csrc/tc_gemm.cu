@@ -33,18 +33,29 @@ constexpr int kRasterGroup = 8;   // M-pairs per raster group (8 x 512 rows of A
 constexpr int kDequantWarp0 = 8;
 constexpr int kDequantWarpsPerStep = 4;   // one of the two producer groups
 constexpr int kEpiWarp0 = 4;
-constexpr size_t kGemmSmemBytes =
-    1024 + (size_t)kStages * (kStageABytes + kStageBBytes) + 8 * (3 * kStages + 2) + 128;
+constexpr int kEpiStageBytes = 32 * 128;   // one staging tile: 32 rows of 128 bytes
+constexpr size_t kGemmSmemBytes = 1024 + (size_t)kStages * (kStageABytes + kStageBBytes) +
+                                  4 * 2 * kEpiStageBytes + 8 * (3 * kStages + 3) + 128;
+static_assert(kGemmSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // Wait-site ids recorded in the device error word when a bounded wait runs out.
 enum : uint32_t { kSiteEmptyTma = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4,
-                  kSiteEmptyDeq = 5, kSitePeerFull = 6, kSiteRelay = 7 };
+                  kSiteEmptyDeq = 5, kSitePeerFull = 6, kSiteRelay = 7, kSiteDrain = 8 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr)
+                 : "memory");
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
@@ -278,73 +289,98 @@ __device__ __forceinline__ DeqJob make_deq_job(const GemmParams& p, const SeqPos
 
 // ----------------------------------------------------------------------------- epilogue
 
-__device__ __forceinline__ void epilogue_store(const Problem& pr, int split, int row, int col0,
-                                               const float (&v)[32]) {
-    if (col0 >= pr.n_valid) return;
+// Epilogue of one warp: its 32 accumulator rows (lane = row row0 + lane) in chunks of 32
+// columns.  bf16 and fp32 outputs go through two alternating 4 KB staging tiles in shared
+// memory (128-byte rows, 16-byte pieces XOR-swizzled by row, the layout of a 128-byte
+// swizzled TMA box) and leave by bulk tensor stores: 64 columns per bf16 tile, 32 per fp32
+// tile.  The stores run in the background, so the accumulator is released as soon as its
+// last chunk is in registers.  The arithmetic per element is alpha * acc, then the residual
+// (bf16) or, for EPI_F32_ACC, the old value added by the bulk reduce (one fp32 addition,
+// commutative), then the rounding.
+struct EpiStage {
+    uint32_t base;   // this warp's two staging tiles
+    uint32_t buf;    // the tile written next
+};
+
+__device__ __forceinline__ void epi_acquire(EpiStage& st, int lane) {
+    if (lane == 0) ptx::bulk_wait_read_1();   // the tile written two stores ago has been read
+    __syncwarp();
+}
+
+__device__ __forceinline__ void epi_release(EpiStage& st, int lane, const CUtensorMap* map, int mode,
+                                           int x, int y, int z) {
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        const uint32_t src = st.base + st.buf * kEpiStageBytes;
+        if (mode == EPI_PARTIAL) ptx::tma_store_3d(map, src, x, y, z);
+        else if (mode == EPI_F32_ACC) ptx::tma_reduce_add_2d(map, src, x, y);
+        else ptx::tma_store_2d(map, src, x, y);
+        ptx::bulk_commit();
+    }
+    __syncwarp();
+    st.buf ^= 1u;
+}
+
+__device__ __forceinline__ void epi_chunk(const Problem& pr, const CUtensorMap* map, int split, int row0,
+                                          int col0, const uint32_t (&r)[32], EpiStage& st, int lane) {
     const float al = pr.alpha;
-    switch (pr.epi) {
-        case EPI_BF16: {
-            uint16_t* o = static_cast<uint16_t*>(pr.out) + (int64_t)row * pr.ldo + col0;
-            const uint16_t* rs = pr.residual ? pr.residual + (int64_t)row * pr.ldr + col0 : nullptr;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (col0 + 8 * g >= pr.n_valid) break;
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = v[8 * g + j] * al;
-                if (rs) {
-                    const uint4 r4 = *reinterpret_cast<const uint4*>(rs + 8 * g);
-                    const uint32_t rr[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        f[2 * j] += __uint_as_float(rr[j] << 16);
-                        f[2 * j + 1] += __uint_as_float(rr[j] & 0xFFFF0000u);
-                    }
-                }
-                uint4 w;
-                w.x = pack_bf16x2(f[0], f[1]);
-                w.y = pack_bf16x2(f[2], f[3]);
-                w.z = pack_bf16x2(f[4], f[5]);
-                w.w = pack_bf16x2(f[6], f[7]);
-                *reinterpret_cast<uint4*>(o + 8 * g) = w;
-            }
-            break;
-        }
-        case EPI_F32:
-        case EPI_F32_ACC:
-        case EPI_PARTIAL: {
-            float* o;
-            float a2 = al;
-            if (pr.epi == EPI_PARTIAL) {
-                o = static_cast<float*>(pr.out) + (int64_t)split * pr.part_stride +
-                    (int64_t)row * pr.ldo + col0;
-                a2 = 1.0f;
-            } else {
-                o = static_cast<float*>(pr.out) + (int64_t)row * pr.ldo + col0;
-            }
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                if (col0 + 4 * g >= pr.n_valid) break;
-                float4 x = make_float4(v[4 * g] * a2, v[4 * g + 1] * a2, v[4 * g + 2] * a2,
-                                       v[4 * g + 3] * a2);
-                if (pr.epi == EPI_F32_ACC) {
-                    const float4 y = *reinterpret_cast<const float4*>(o + 4 * g);
-                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                }
-                *reinterpret_cast<float4*>(o + 4 * g) = x;
-            }
-            break;
-        }
-        case EPI_F32_T: {
+    if (pr.epi == EPI_F32_T) {
+        // transposed output: for a fixed column the lanes write consecutive rows
+        const int row = row0 + lane;
+        if (row < pr.m && col0 < pr.n_valid) {
             float* o = static_cast<float*>(pr.out);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < pr.n_valid) o[(int64_t)(col0 + j) * pr.ldo + row] = v[j] * al;
-            break;
+                if (col0 + j < pr.n_valid) o[(int64_t)(col0 + j) * pr.ldo + row] = __uint_as_float(r[j]) * al;
         }
-        default:
-            break;
+        __syncwarp();
+        return;
     }
+    const uint32_t swz = (uint32_t)(lane & 7);
+    if (pr.epi == EPI_BF16) {
+        const int half = (col0 >> 5) & 1;   // which 32 columns of the 64-column tile
+        const int tcol = col0 - 32 * half;
+        // warp-uniform: a second half wholly past the valid columns was left out when the
+        // tile was stored after its first half
+        if (col0 >= pr.n_valid) return;
+        if (half == 0) epi_acquire(st, lane);
+        const int row = row0 + lane;
+        const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[8 * g + j]) * al;
+            if (pr.residual && row < pr.m && col0 + 8 * g < pr.n_valid) {
+                const uint4 r4 = *reinterpret_cast<const uint4*>(pr.residual + (int64_t)row * pr.ldr + col0 + 8 * g);
+                const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f[2 * j] += __uint_as_float(rw[j] << 16);
+                    f[2 * j + 1] += __uint_as_float(rw[j] & 0xFFFF0000u);
+                }
+            }
+            st_shared_v4(dst + ((((uint32_t)(4 * half + g)) ^ swz) << 4), pack_bf16x2(f[0], f[1]),
+                         pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+        // the tile leaves after its second half, or after the first when the second half
+        // lies wholly past the valid columns (the box is clipped there anyway)
+        if (half == 1 || col0 + 32 >= pr.n_valid) epi_release(st, lane, map, EPI_BF16, tcol, row0, 0);
+        else __syncwarp();
+        return;
+    }
+    if (col0 >= pr.n_valid) return;   // warp-uniform
+    epi_acquire(st, lane);
+    const float a2 = pr.epi == EPI_PARTIAL ? 1.0f : al;
+    const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        st_shared_v4(dst + ((((uint32_t)g) ^ swz) << 4), __float_as_uint(__uint_as_float(r[4 * g]) * a2),
+                     __float_as_uint(__uint_as_float(r[4 * g + 1]) * a2),
+                     __float_as_uint(__uint_as_float(r[4 * g + 2]) * a2),
+                     __float_as_uint(__uint_as_float(r[4 * g + 3]) * a2));
+    epi_release(st, lane, map, pr.epi, col0, row0, split);
 }
 
 // ------------------------------------------------------------------------------ kernel
@@ -356,13 +392,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     uint8_t* const gbase = smem_raw + (base - raw);
     const uint32_t sA = base;
     const uint32_t sB = base + kStages * kStageABytes;
-    const uint32_t sBar = sB + kStages * kStageBBytes;
+    const uint32_t sStg = sB + kStages * kStageBBytes;   // epilogue staging, two tiles per warp
+    const uint32_t sBar = sStg + 4 * 2 * kEpiStageBytes;
     auto full_bar = [&](int s) { return sBar + 8u * s; };
     auto pfull_bar = [&](int s) { return sBar + 8u * (kStages + s); };
     auto empty_bar = [&](int s) { return sBar + 8u * (2 * kStages + s); };
     const uint32_t acc_full = sBar + 8u * (3 * kStages);
     const uint32_t acc_empty = acc_full + 8u;
-    uint8_t* const gmisc = gbase + (sBar - base) + 8 * (3 * kStages + 2);
+    const uint32_t drain_bar = acc_empty + 8u;   // the issuer's own MMAs have all finished
+    uint8_t* const gmisc = gbase + (sBar - base) + 8 * (3 * kStages + 3);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc + 4);
 
@@ -379,6 +417,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         }
         ptx::mbar_init(acc_full, 1);
         ptx::mbar_init(acc_empty, 256);   // both CTAs' epilogue threads (used in the even CTA)
+        ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -488,6 +527,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 ptx::umma_commit_pair_mc(acc_full, 0x3);
                 acc_phase ^= 1u;
             }
+            // Every pair MMA this thread issued has finished before the CTAs may release
+            // TMEM and shared memory, on the normal path and after an abort alike.
+            ptx::umma_commit_pair_mc(drain_bar, 0x1);
+            volatile int no_abort = 0;   // this wait does not end early on an abort
+            if (!ptx::mbar_wait_bounded(drain_bar, 0, &no_abort, p.err, kSiteDrain)) *abort_flag = 1;
         }
     } else if (warp == 2) {
         // ------------------------------------------- relay of stage readiness (rank 1)
@@ -506,29 +550,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         const int q = warp - kEpiWarp0;
         uint32_t acc_phase = 0;
         const uint32_t acc_empty_dst = leader ? acc_empty : ptx::mapa(acc_empty, 0);
+        EpiStage est{sStg + (uint32_t)q * 2u * kEpiStageBytes, 0u};
         for (int t = (int)ptx::cluster_id_x(); t < p.total_tiles; t += (int)ptx::n_clusters_x()) {
             const TileInfo ti = decode_tile(p, t, rank);
             const TileInfo t0 = decode_tile(p, t, 0);   // which blocks the pair MMAs wrote
             const Problem& pr = p.probs[ti.prob];
+            const CUtensorMap* omap = &p.out_maps[ti.prob];
             int ok = 0;
             if (lane == 0) ok = ptx::mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.err, kSiteAccFull);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after();
-            for (int h = 0; h < 2; ++h) {
-                if ((h == 0 && !t0.half0) || (h == 1 && !t0.half1)) continue;
-                const int row = ti.m0 + h * 128 + q * 32 + lane;
-                for (int c = 0; c < pr.bn; c += 32) {
-                    float v[32];
-                    ptx::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * pr.bn + c), v);
-                    if (row < pr.m) epilogue_store(pr, ti.split, row, ti.n0 + c, v);
-                }
+            // chunks of 32 columns over both 128-row blocks; the TMEM load of the next chunk
+            // is in flight while the current one is staged (tcgen05.ld and its wait are
+            // warp-collective: every path through epi_chunk ends reconverged)
+            const int h_first = t0.half0 ? 0 : 1, h_last = t0.half1 ? 1 : 0;
+            const int per_h = pr.bn / 32;
+            const int n_chunks = (h_last - h_first + 1) * per_h;
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+            auto chunk_h = [&](int i) { return h_first + i / per_h; };
+            auto chunk_c = [&](int i) { return (i % per_h) * 32; };
+            uint32_t ra[32], rb[32];
+            __syncwarp();
+            ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * pr.bn + chunk_c(0)), ra);
+            ptx::tmem_ld_wait(ra);
+            for (int i = 0; i < n_chunks; i += 2) {
+                if (i + 1 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
+                epi_chunk(pr, omap, ti.split, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane);
+                if (i + 1 >= n_chunks) break;
+                ptx::tmem_ld_wait(rb);
+                if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * pr.bn + chunk_c(i + 2)), ra);
+                epi_chunk(pr, omap, ti.split, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est,
+                          lane);
+                if (i + 2 < n_chunks) ptx::tmem_ld_wait(ra);
             }
             ptx::tc_fence_before();
             if (leader) ptx::mbar_arrive(acc_empty_dst);
             else ptx::mbar_arrive_remote(acc_empty_dst);
             acc_phase ^= 1u;
         }
+        // the bulk stores read shared memory and write the output: both end before the CTA does
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
     } else if (warp >= kDequantWarp0) {
         // --------------------------------------------------------------- B producer
         // Two groups of four warps take alternate k-steps of the sequence, so two k-steps
@@ -593,12 +656,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     }
 
     __syncthreads();
+    // An abort in either CTA is an abort of the pair: tell the peer, then both settle.
+    if (threadIdx.x == 0 && *abort_flag)
+        ptx::st_cluster_u32(ptx::mapa(ptx::smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u), 1u);
+    ptx::cluster_sync();   // no CTA leaves while the pair may still use its memory
     if (*abort_flag) {
-        // let copies and MMAs already in flight land before the CTA releases its resources
+        // let copies already in flight land before the CTAs release their resources
         if (threadIdx.x == 0) ptx::settle_ns(50000);
         __syncthreads();
+        ptx::cluster_sync();
     }
-    ptx::cluster_sync();   // no CTA leaves while the pair may still use its memory
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem, 512);
@@ -761,6 +828,39 @@ static int max_pair_clusters() {
     }
     cached[dev] = n;
     return n;
+}
+
+// Output tensor map of a problem for the bulk-store epilogue: bf16 boxes of 64 x 32, fp32
+// boxes of 32 x 32 (128-byte rows, 128-byte swizzle), clipped at m rows and n_valid columns;
+// split-K partials as a 3-D tensor [split][m][n] so that each split is clipped on its own.
+static int encode_out_map(const Problem& pr, CUtensorMap* map) {
+    if (pr.epi == EPI_F32_T) return LSN_OK;   // written directly
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(LSN_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    const bool bf = pr.epi == EPI_BF16;
+    const int64_t es = bf ? 2 : 4;
+    if ((pr.ldo * es) % 16 || pr.ldo < pr.n_valid)
+        return fail(LSN_EINVAL, "gemm: output rows must be 16-byte multiples");
+    CUresult r;
+    if (pr.epi == EPI_PARTIAL) {
+        cuuint64_t dims[3] = {(cuuint64_t)pr.n, (cuuint64_t)pr.m, (cuuint64_t)pr.splits};
+        cuuint64_t strides[2] = {(cuuint64_t)(pr.ldo * 4), (cuuint64_t)(pr.part_stride * 4)};
+        cuuint32_t box[3] = {32u, 32u, 1u};
+        cuuint32_t est[3] = {1u, 1u, 1u};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pr.out, dims, strides, box, est,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[2] = {(cuuint64_t)pr.n_valid, (cuuint64_t)pr.m};
+        cuuint64_t strides[1] = {(cuuint64_t)(pr.ldo * es)};
+        cuuint32_t box[2] = {bf ? 64u : 32u, 32u};
+        cuuint32_t est[2] = {1u, 1u};
+        r = enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pr.out, dims,
+                strides, box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return fail(LSN_ECUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+    return LSN_OK;
 }
 
 int choose_splits(int64_t units, int ksteps) {
@@ -934,6 +1034,10 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
         }
     }
     p_.total_tiles = tiles;
+    for (int i = 0; i < p_.n_probs; ++i) {
+        int rc = encode_out_map(p_.probs[i], &p_.out_maps[i]);
+        if (rc) return status_ = rc;
+    }
     memcpy(p_.levels, nf4_levels(), sizeof(p_.levels));
     p_.err = ext_err_ ? ext_err_ : device_error_word();
     if (!p_.err) return LSN_ECUDA;

@@ -89,6 +89,7 @@ struct Nf4Dev {
 
 struct GemmParams {   // 128-byte aligned through CUtensorMap
     CUtensorMap maps[kMaxMaps];
+    CUtensorMap out_maps[kMaxProbs];   // per problem: the output for the bulk-store epilogue
     Nf4Dev nf4[kMaxNf4];
     KSeg segs[kMaxSegs];
     Problem probs[kMaxProbs];

@@ -159,4 +159,5 @@ def test_accumulate_dx_and_zero_A_gives_zero_dB():
     dX2 = dX1.clone()
     lsn.lora_nf4_bwd(packed, N, K, X, T, dY, A0, B, 8, 2.0, dX=dX2, accumulate_dX=True)
     torch.cuda.synchronize()
-    assert torch.allclose(dX2, 2 * dX1, rtol=1e-6, atol=1e-6)
+    # one fp32 addition per element of the same deterministic dX: exactly twice dX1
+    assert torch.equal(dX2, 2 * dX1)
