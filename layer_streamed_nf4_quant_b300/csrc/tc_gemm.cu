@@ -42,11 +42,12 @@ static_assert(kGemmSmemBytes <= 227 * 1024, "shared memory per CTA");
 enum : uint32_t { kSiteEmptyTma = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4,
                   kSiteEmptyDeq = 5, kSitePeerFull = 6, kSiteRelay = 7, kSiteDrain = 8 };
 
+// No "memory" clobber: the store stays ordered with the other volatile asm statements (the
+// proxy fence, the barrier arrives), and the compiler may keep values it loaded from the
+// kernel parameters in registers across it instead of reloading them after every store.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -322,38 +323,64 @@ __device__ __forceinline__ void epi_release(EpiStage& st, int lane, const CUtens
     st.buf ^= 1u;
 }
 
-__device__ __forceinline__ void epi_chunk(const Problem& pr, const CUtensorMap* map, int split, int row0,
-                                          int col0, const uint32_t (&r)[32], EpiStage& st, int lane) {
-    const float al = pr.alpha;
-    if (pr.epi == EPI_F32_T) {
+// The per-problem values the epilogue needs, copied into registers once per tile.
+struct EpiArgs {
+    int epi, m, n_valid, split;
+    float alpha;
+    void* out;
+    int64_t ldo;
+    const uint16_t* residual;
+    int64_t ldr;
+};
+
+__device__ __forceinline__ EpiArgs epi_args(const Problem& pr, int split) {
+    EpiArgs a;
+    a.epi = pr.epi;
+    a.m = pr.m;
+    a.n_valid = pr.n_valid;
+    a.split = split;
+    a.alpha = pr.alpha;
+    a.out = pr.out;
+    a.ldo = pr.ldo;
+    a.residual = pr.residual;
+    a.ldr = pr.ldr;
+    return a;
+}
+
+__device__ __forceinline__ void epi_chunk(const EpiArgs& a, const CUtensorMap* map, int row0, int col0,
+                                          const uint32_t (&r)[32], EpiStage& st, int lane) {
+    const float al = a.alpha;
+    if (a.epi == EPI_F32_T) {
         // transposed output: for a fixed column the lanes write consecutive rows
         const int row = row0 + lane;
-        if (row < pr.m && col0 < pr.n_valid) {
-            float* o = static_cast<float*>(pr.out);
+        if (row < a.m && col0 < a.n_valid) {
+            float* o = static_cast<float*>(a.out);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < pr.n_valid) o[(int64_t)(col0 + j) * pr.ldo + row] = __uint_as_float(r[j]) * al;
+                if (col0 + j < a.n_valid) o[(int64_t)(col0 + j) * a.ldo + row] = __uint_as_float(r[j]) * al;
         }
         __syncwarp();
         return;
     }
     const uint32_t swz = (uint32_t)(lane & 7);
-    if (pr.epi == EPI_BF16) {
+    if (a.epi == EPI_BF16) {
         const int half = (col0 >> 5) & 1;   // which 32 columns of the 64-column tile
         const int tcol = col0 - 32 * half;
         // warp-uniform: a second half wholly past the valid columns was left out when the
         // tile was stored after its first half
-        if (col0 >= pr.n_valid) return;
+        if (col0 >= a.n_valid) return;
         if (half == 0) epi_acquire(st, lane);
         const int row = row0 + lane;
         const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
+        const bool res_row = a.residual != nullptr && row < a.m;
+        const uint16_t* rp = res_row ? a.residual + (int64_t)row * a.ldr + col0 : nullptr;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             float f[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[8 * g + j]) * al;
-            if (pr.residual && row < pr.m && col0 + 8 * g < pr.n_valid) {
-                const uint4 r4 = *reinterpret_cast<const uint4*>(pr.residual + (int64_t)row * pr.ldr + col0 + 8 * g);
+            if (res_row && col0 + 8 * g < a.n_valid) {
+                const uint4 r4 = *reinterpret_cast<const uint4*>(rp + 8 * g);
                 const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -366,13 +393,13 @@ __device__ __forceinline__ void epi_chunk(const Problem& pr, const CUtensorMap* 
         }
         // the tile leaves after its second half, or after the first when the second half
         // lies wholly past the valid columns (the box is clipped there anyway)
-        if (half == 1 || col0 + 32 >= pr.n_valid) epi_release(st, lane, map, EPI_BF16, tcol, row0, 0);
+        if (half == 1 || col0 + 32 >= a.n_valid) epi_release(st, lane, map, EPI_BF16, tcol, row0, 0);
         else __syncwarp();
         return;
     }
-    if (col0 >= pr.n_valid) return;   // warp-uniform
+    if (col0 >= a.n_valid) return;   // warp-uniform
     epi_acquire(st, lane);
-    const float a2 = pr.epi == EPI_PARTIAL ? 1.0f : al;
+    const float a2 = a.epi == EPI_PARTIAL ? 1.0f : al;
     const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
 #pragma unroll
     for (int g = 0; g < 8; ++g)
@@ -380,7 +407,7 @@ __device__ __forceinline__ void epi_chunk(const Problem& pr, const CUtensorMap* 
                      __float_as_uint(__uint_as_float(r[4 * g + 1]) * a2),
                      __float_as_uint(__uint_as_float(r[4 * g + 2]) * a2),
                      __float_as_uint(__uint_as_float(r[4 * g + 3]) * a2));
-    epi_release(st, lane, map, pr.epi, col0, row0, split);
+    epi_release(st, lane, map, a.epi, col0, row0, a.split);
 }
 
 // ------------------------------------------------------------------------------ kernel
@@ -485,6 +512,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             seq_begin(p, s, rank);
             uint32_t acc_phase = 0;
             uint32_t i = 0;
+            // Operand descriptors at stage 0; the start-address field (address / 16, bits 0-13)
+            // takes the stage, block and k16 offsets by plain addition (shared memory < 256 KB).
+            const uint64_t dA_k = ptx::smem_desc_sw128(sA, 16, 1024), dA_mn = ptx::smem_desc_sw128(sA, 8192, 1024);
+            const uint64_t dB_k = ptx::smem_desc_sw128(sB, 16, 1024), dB_mn = ptx::smem_desc_sw128(sB, 8192, 1024);
+            constexpr uint32_t kHalfA16 = (kStageABytes / 2) >> 4;   // the second 128-row block
             while (s.t < p.total_tiles) {
                 const int t = s.t;
                 const TileInfo ti = s.ti;
@@ -493,6 +525,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                     break;
                 ptx::tc_fence_after();
                 const bool a_mn = pr.a_major == A_MNMAJOR;
+                const uint64_t dA = a_mn ? dA_mn : dA_k;
+                const uint32_t a_k16 = a_mn ? (2048u >> 4) : (32u >> 4);
+                const uint32_t idesc_bk = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, 0, 256);
+                const uint32_t idesc_bmn = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, 1, 256);
+                const uint32_t tmem_h1 = tmem + (uint32_t)pr.bn;
+                const bool h0 = ti.half0, h1 = ti.half1;
                 bool ok = true;
                 for (; s.t == t; ++i, seq_next(p, s, rank)) {
                     const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
@@ -503,23 +541,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                     }
                     ptx::tc_fence_after();
                     const bool b_mn = seg_b_mn(p.segs[s.si].b_src);
-                    const uint32_t idesc = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, b_mn ? 1 : 0, 256);
-                    const uint32_t a_base = sA + stage * kStageABytes;
-                    const uint32_t b_base = sB + stage * kStageBBytes;
+                    const uint32_t idesc = b_mn ? idesc_bmn : idesc_bk;
+                    const uint64_t a0 = dA + ((stage * (uint32_t)kStageABytes) >> 4);
+                    const uint64_t b0 = (b_mn ? dB_mn : dB_k) + ((stage * (uint32_t)kStageBBytes) >> 4);
+                    const uint32_t b_k16 = b_mn ? (2048u >> 4) : (32u >> 4);
+                    const bool first = s.ks == ti.ks_begin;
 #pragma unroll
                     for (int k4 = 0; k4 < kBK / 16; ++k4) {
-                        const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(b_base + k4 * 2048, 8192, 1024)
-                                                    : ptx::smem_desc_sw128(b_base + k4 * 32, 16, 1024);
-                        const uint32_t acc = (s.ks > ti.ks_begin || k4 > 0) ? 1u : 0u;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            // rows of block h: 128 of this CTA's tile and 128 of the peer's
-                            if ((h == 0 && !ti.half0) || (h == 1 && !ti.half1)) continue;
-                            const uint32_t ab = a_base + h * (kStageABytes / 2);
-                            const uint64_t adesc = a_mn ? ptx::smem_desc_sw128(ab + k4 * 2048, 8192, 1024)
-                                                        : ptx::smem_desc_sw128(ab + k4 * 32, 16, 1024);
-                            ptx::umma_f16_pair(tmem + (uint32_t)(h * pr.bn), adesc, bdesc, idesc, acc);
-                        }
+                        // rows of block h: 128 of this CTA's tile and 128 of the peer's
+                        const uint64_t bd = b0 + (uint64_t)(k4 * b_k16);
+                        const uint64_t ad = a0 + (uint64_t)(k4 * a_k16);
+                        const uint32_t acc = (first && k4 == 0) ? 0u : 1u;
+                        if (h0) ptx::umma_f16_pair(tmem, ad, bd, idesc, acc);
+                        if (h1) ptx::umma_f16_pair(tmem_h1, ad + kHalfA16, bd, idesc, acc);
                     }
                     ptx::umma_commit_pair_mc(empty_bar(stage), 0x3);
                 }
@@ -556,6 +590,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             const TileInfo t0 = decode_tile(p, t, 0);   // which blocks the pair MMAs wrote
             const Problem& pr = p.probs[ti.prob];
             const CUtensorMap* omap = &p.out_maps[ti.prob];
+            const EpiArgs ea = epi_args(pr, ti.split);
             int ok = 0;
             if (lane == 0) ok = ptx::mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.err, kSiteAccFull);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -576,12 +611,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             ptx::tmem_ld_wait(ra);
             for (int i = 0; i < n_chunks; i += 2) {
                 if (i + 1 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
-                epi_chunk(pr, omap, ti.split, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane);
+                epi_chunk(ea, omap, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane);
                 if (i + 1 >= n_chunks) break;
                 ptx::tmem_ld_wait(rb);
                 if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * pr.bn + chunk_c(i + 2)), ra);
-                epi_chunk(pr, omap, ti.split, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est,
-                          lane);
+                epi_chunk(ea, omap, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est, lane);
                 if (i + 2 < n_chunks) ptx::tmem_ld_wait(ra);
             }
             ptx::tc_fence_before();

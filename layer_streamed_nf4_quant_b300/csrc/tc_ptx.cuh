@@ -51,21 +51,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Cluster-scope acquire form of the parity wait: used where the arrivals come from the peer
-// CTA of the cluster (remote arrives, multicast commits).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+// CTA of the cluster (remote arrives, multicast commits).  The thread is suspended until the
+// phase completes or about suspend_ns have passed, so waiting roles do not take issue slots
+// from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity, uint32_t suspend_ns = 0) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
 
-// Wait budget of one bounded wait (nanoseconds of %globaltimer).
+// Wait budget of one bounded wait (nanoseconds of %globaltimer), and the suspend time asked
+// of each try_wait inside it (an abort by another role is noticed within about that time).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitSuspendNs = 20000u;
 
 // Waits until the phase with the given parity has completed.  Gives up (returns false) when
 // *abort is set by another role or after kWaitLimitNs; in the latter case it sets *abort and
@@ -75,15 +79,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint32_t site) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                if (err) atomicCAS(err, 0u, (1u << 24) | site);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity, kWaitSuspendNs)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            if (err) atomicCAS(err, 0u, (1u << 24) | site);
+            return false;
         }
     }
 }
