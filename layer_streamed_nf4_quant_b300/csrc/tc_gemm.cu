@@ -373,12 +373,13 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& a, const CUtensorMap* m
         const int row = row0 + lane;
         const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
         const bool res_row = a.residual != nullptr && row < a.m;
+        const bool unit = al == 1.0f;   // x * 1.0f == x exactly, so the multiply is skipped
         const uint16_t* rp = res_row ? a.residual + (int64_t)row * a.ldr + col0 : nullptr;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             float f[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[8 * g + j]) * al;
+            for (int j = 0; j < 8; ++j) f[j] = unit ? __uint_as_float(r[8 * g + j]) : __uint_as_float(r[8 * g + j]) * al;
             if (res_row && col0 + 8 * g < a.n_valid) {
                 const uint4 r4 = *reinterpret_cast<const uint4*>(rp + 8 * g);
                 const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
@@ -600,11 +601,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             // is in flight while the current one is staged (tcgen05.ld and its wait are
             // warp-collective: every path through epi_chunk ends reconverged)
             const int h_first = t0.half0 ? 0 : 1, h_last = t0.half1 ? 1 : 0;
-            const int per_h = pr.bn / 32;
-            const int n_chunks = (h_last - h_first + 1) * per_h;
+            const int per_h_log = pr.bn == 256 ? 3 : 2;   // 32-column chunks per block: bn / 32
+            const int n_chunks = (h_last - h_first + 1) << per_h_log;
             const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-            auto chunk_h = [&](int i) { return h_first + i / per_h; };
-            auto chunk_c = [&](int i) { return (i % per_h) * 32; };
+            auto chunk_h = [&](int i) { return h_first + (i >> per_h_log); };
+            auto chunk_c = [&](int i) { return (i & ((1 << per_h_log) - 1)) * 32; };
             uint32_t ra[32], rb[32];
             __syncwarp();
             ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * pr.bn + chunk_c(0)), ra);
