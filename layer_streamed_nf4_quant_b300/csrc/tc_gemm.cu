@@ -29,7 +29,7 @@ namespace lsn {
 
 static_assert(sizeof(GemmParams) <= 32764, "kernel parameters must fit the 32 KB limit");
 
-constexpr int kRasterGroup = 8;   // M-pairs per raster group (8 x 512 rows of A)
+constexpr int kRasterGroup = 8;   // at most this many M-pairs per raster group
 constexpr int kDequantWarp0 = 8;
 constexpr int kDequantWarpsPerStep = 4;   // one of the two producer groups
 constexpr int kEpiWarp0 = 4;
@@ -159,12 +159,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, uint
     const int per_split = pr.tiles_m * pr.tiles_n;   // tiles_m counts M-pairs
     const int s = l / per_split;
     const int r = l - s * per_split;
-    // grouped raster: kRasterGroup M-pairs sweep all N tiles together, so the A rows of the
+    // grouped raster: pr.raster M-pairs sweep all N tiles together, so the A rows of the
     // group stay in L2 while B streams past them once per group
-    const int g = r / (kRasterGroup * pr.tiles_n);
-    const int first_m = g * kRasterGroup;
-    const int gm = min(kRasterGroup, pr.tiles_m - first_m);
-    const int rr = r - g * kRasterGroup * pr.tiles_n;
+    const int rg = pr.raster;
+    const int g = r / (rg * pr.tiles_n);
+    const int first_m = g * rg;
+    const int gm = min(rg, pr.tiles_m - first_m);
+    const int rr = r - g * rg * pr.tiles_n;
     const int nt = rr / gm;
     const int mt = first_m + (rr - nt * gm);
     TileInfo ti;
@@ -1053,6 +1054,15 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
         if (pr.splits > pr.ksteps) pr.splits = pr.ksteps;
         pr.tiles_m = ((pr.m + kBM - 1) / kBM + 1) / 2;   // M-pairs: one per CTA pair
         pr.tiles_n = (pr.n + pr.bn - 1) / pr.bn;
+        // raster group: as many M-pairs as keep their A rows (512 x K bf16 each) within
+        // about 48 MB of L2, between 1 and kRasterGroup
+        {
+            int64_t k_total = 0;
+            for (int j = 0; j < pr.seg_count; ++j) k_total += p_.segs[pr.seg_begin + j].k_len;
+            const int64_t a_pair = 2 * (int64_t)kBM * k_total * 2;
+            int rg = (int)((48ll << 20) / (a_pair > 0 ? a_pair : 1));
+            pr.raster = rg < 1 ? 1 : (rg > kRasterGroup ? kRasterGroup : rg);
+        }
         pr.tile_begin = tiles;
         tiles += pr.tiles_m * pr.tiles_n * pr.splits;
         fin[i] = {pr.epi, pr.out, pr.ldo, pr.alpha, pr.residual, pr.ldr};

@@ -68,6 +68,7 @@ struct Problem {
     int ksteps;        // total over the segments
     int splits;
     int tiles_m, tiles_n;
+    int raster;        // M-pairs per raster group (set at launch)
     int tile_begin;
     int epi;
     void* out;
