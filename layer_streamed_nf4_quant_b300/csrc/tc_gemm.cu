@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             uint32_t n_steps = 0;
             for (uint32_t i = 0; s.t < p.total_tiles; ++i, seq_next(p, s, rank)) {
                 const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
-                if (!ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyTma))
+                if (!ptx::mbar_wait_bounded_cta(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyTma))
                     break;
                 const Problem& pr = p.probs[s.ti.prob];
                 const KSeg& sg = p.segs[s.si];
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             if (!*abort_flag) {
                 for (uint32_t st = 0; st < (uint32_t)kStages && st < n_steps; ++st) {
                     const uint32_t last = st + ((n_steps - 1 - st) / kStages) * kStages;
-                    if (!ptx::mbar_wait_bounded(empty_bar(st), (last / kStages) & 1u, abort_flag, p.err,
+                    if (!ptx::mbar_wait_bounded_cta(empty_bar(st), (last / kStages) & 1u, abort_flag, p.err,
                                                 kSiteEmptyTma))
                         break;
                 }
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 bool ok = true;
                 for (; s.t == t; ++i, seq_next(p, s, rank)) {
                     const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
-                    if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteFull) ||
+                    if (!ptx::mbar_wait_bounded_cta(full_bar(stage), phase, abort_flag, p.err, kSiteFull) ||
                         !ptx::mbar_wait_bounded(pfull_bar(stage), phase, abort_flag, p.err, kSitePeerFull)) {
                         ok = false;
                         break;
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             seq_begin(p, s, rank);
             for (uint32_t i = 0; s.t < p.total_tiles; ++i, seq_next(p, s, rank)) {
                 const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
-                if (!ptx::mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.err, kSiteRelay)) break;
+                if (!ptx::mbar_wait_bounded_cta(full_bar(stage), phase, abort_flag, p.err, kSiteRelay)) break;
                 ptx::mbar_arrive_remote(remote_pfull0 + 8u * stage);
             }
         }
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
             int ok = 0;
             if (lane == 0)
-                ok = ptx::mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
+                ok = ptx::mbar_wait_bounded_cta(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (cur.kind != kJobNone) {

@@ -38,14 +38,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// CTA-scope acquire form (the default): for barriers whose arrivals carry no memory writes
+// of another CTA that the waiting side reads (stage-full of this CTA's own copies and
+// producers; stage-empty, released by MMA completion).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns = 0) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
@@ -74,13 +77,17 @@ constexpr uint32_t kWaitSuspendNs = 20000u;
 // Waits until the phase with the given parity has completed.  Gives up (returns false) when
 // *abort is set by another role or after kWaitLimitNs; in the latter case it sets *abort and
 // records (kind 1, site) in the device error word.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, uint32_t* err,
-                                                  uint32_t site) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_wait_bounded_scoped(uint32_t bar, uint32_t parity,
+                                                         volatile int* abort, uint32_t* err,
+                                                         uint32_t site) {
+    auto try_wait = [&](uint32_t ns) {
+        return kClusterScope ? mbar_try_wait_cluster(bar, parity, ns) : mbar_try_wait(bar, parity, ns);
+    };
+    if (try_wait(0)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        if (mbar_try_wait_cluster(bar, parity, kWaitSuspendNs)) return true;
+        if (try_wait(kWaitSuspendNs)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort = 1;
@@ -88,6 +95,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
             return false;
         }
     }
+}
+// Cluster-scope acquire: arrivals from the peer CTA (remote arrives, multicast commits).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t* err, uint32_t site) {
+    return mbar_wait_bounded_scoped<true>(bar, parity, abort, err, site);
+}
+// CTA-scope acquire (see mbar_try_wait).
+__device__ __forceinline__ bool mbar_wait_bounded_cta(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                      uint32_t* err, uint32_t site) {
+    return mbar_wait_bounded_scoped<false>(bar, parity, abort, err, site);
 }
 
 // Busy-waits for a fixed time (bounded); used on the abort path to let copies and MMAs
