@@ -10,14 +10,17 @@
 // in HBM.  The LoRA branch enters as extra contraction steps of the same accumulator
 // (s*T*B^T forward, dT*A backward), so one fp32 TMEM accumulator holds the full result.
 //
-// CTA roles (512 threads, one CTA per SM, persistent over a static tile order):
+// Clusters of two CTAs (one per SM) share each tile through cta_group::2 MMAs; persistent
+// over a static tile order.  CTA roles (512 threads):
 //   warp 0       TMA producer of A (and of dense B) tiles
-//   warp 1       TMEM allocator and single-thread UMMA issuer
-//   warps 4-7    epilogue: TMEM -> registers -> global
+//   warp 1       TMEM allocator (both CTAs) and, in the even CTA, the single-thread UMMA issuer
+//   warp 2       in the odd CTA: relays "stage full" to the even CTA
+//   warps 4-7    epilogue: TMEM -> registers -> swizzled shared staging -> bulk tensor stores
 //   warps 8-15   B producer: NF4 decode / scaled LoRA-B rows into shared memory
 // Every tile has a fixed K order and a fixed owner; split-K partials are reduced in split
-// order by gemm_reduce.  No atomics touch results, so every launch is bit-reproducible and
-// independent of where the weights live.
+// order by gemm_reduce; the accumulate mode adds through the bulk reduce, one addition per
+// output element per launch.  So every launch is bit-reproducible and independent of where
+// the weights live.
 #include <cuda_bf16.h>
 #include <string.h>
 
@@ -48,15 +51,6 @@ enum : uint32_t { kSiteEmptyTma = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccF
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d));
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(addr)
-                 : "memory");
-    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
