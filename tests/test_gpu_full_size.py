@@ -1,0 +1,84 @@
+"""GPU parity at the full token count of the 8 x 2048-token workload (M = 16384), checked
+where the oracle cannot run the whole problem:
+
+* sampled rows: the layer stack is row-independent apart from the normalisation of its
+  means, so x_1 and dx0 on 256 sampled rows are compared with the oracle run on those rows
+  alone (the oracle divides its means by the full M);
+* additivity over rows: every loss term is a mean over rows, so the gradients of the full
+  run equal the sum of the gradients of 64 runs over disjoint 256-row slices, each scaled
+  by 256 / M, and the loss equals the mean of the slice losses.
+
+The launch configuration (tiles, splits, raster) is the one the 16384-token bench uses.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from test_gpu_stack import FWD_TOL, GRAD_TOL, Stack, _bits, _grad_views, _oracle  # noqa: E402
+
+M_FULL = 16384
+SLICE = 256
+
+
+def _lsn():
+    import layer_streamed_nf4_quant_b300 as lsn
+    return lsn
+
+
+@pytest.fixture(scope="module")
+def full():
+    lsn = _lsn()
+    st = Stack(lsn.StackDesc(n_layers=1), M=M_FULL)
+    return st, st.run()
+
+
+def test_sampled_rows_match_oracle(full):
+    from oracle.nf4 import bf16_value
+    st, out = full
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, SLICE - 1, SLICE, M_FULL // 2, M_FULL - 1],
+                                     rng.choice(M_FULL, SLICE - 6, replace=False)]))
+    ref = _oracle(st, rows)
+    x = bf16_value(_bits(out["x"])[rows]).astype(np.float64)
+    assert np.max(np.abs(x - ref["x_last"])) / np.max(np.abs(ref["x_last"])) <= FWD_TOL
+    dx0 = out["dx0"].double().cpu().numpy()[rows]
+    assert np.linalg.norm(dx0 - ref["dx0"]) / np.linalg.norm(ref["dx0"]) <= GRAD_TOL
+
+
+def test_gradients_add_up_over_row_slices(full):
+    lsn = _lsn()
+    st, out = full
+    d = st.desc
+    ws = torch.empty(d.workspace_bytes(SLICE), dtype=torch.uint8, device="cuda")
+    g_sum = torch.zeros(d.lora_elems, dtype=torch.float64, device="cuda")
+    losses = []
+    dx0_slices = []
+    for j in range(M_FULL // SLICE):
+        x0 = st.x0[j * SLICE:(j + 1) * SLICE].contiguous()
+        g = [torch.empty(d.lora_elems, dtype=torch.float32, device="cuda")]
+        loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+        dx0 = torch.empty((SLICE, d.d_model), dtype=torch.float32, device="cuda")
+        lsn.layer_stack_step(d, x0, st.lora, g, loss, ws, resident_store=st.resident, dx0=dx0)
+        torch.cuda.synchronize()
+        g_sum += g[0].double()
+        losses.append(loss.item())
+        if j in (0, M_FULL // SLICE - 1):
+            dx0_slices.append((j, dx0.double()))
+    assert lsn.device_check() == 0
+    scale = SLICE / M_FULL
+    full_g = out["grads"][0].double()
+    want = (g_sum * scale)
+    gA, gB = _grad_views(st, full_g)
+    wA, wB = _grad_views(st, want.float())
+    for p in gA:
+        for got, ref in ((gA[p], wA[p]), (gB[p], wB[p])):
+            assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= GRAD_TOL, p
+    assert abs(out["loss"].item() - np.mean(losses)) / out["loss"].item() <= 1e-4
+    # dx0 rows: the slice's seed gradient is M / SLICE (a power of two) times the full one
+    full_dx0 = out["dx0"].double()
+    for j, dxs in dx0_slices:
+        got = full_dx0[j * SLICE:(j + 1) * SLICE]
+        ref = dxs * scale
+        assert (torch.linalg.norm(got - ref) / torch.linalg.norm(ref)).item() <= GRAD_TOL
