@@ -406,6 +406,47 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& a, const CUtensorMap* m
     epi_release(st, lane, map, a.epi, col0, row0, a.split);
 }
 
+// bf16 output, two chunks (64 columns, one staging tile) at once: all 32 packed words are
+// computed before the shared-memory stores, so the two halves' conversions overlap; one
+// fence and one bulk store per tile.  Same arithmetic as epi_chunk.
+__device__ __forceinline__ void epi_pair_bf16(const EpiArgs& a, const CUtensorMap* map, int row0, int col0,
+                                              const uint32_t (&ra)[32], const uint32_t (&rb)[32], EpiStage& st,
+                                              int lane) {
+    if (col0 >= a.n_valid) return;   // warp-uniform
+    epi_acquire(st, lane);
+    const float al = a.alpha;
+    const bool unit = al == 1.0f;   // x * 1.0f == x exactly, so the multiply is skipped
+    const int row = row0 + lane;
+    const bool res_row = a.residual != nullptr && row < a.m;
+    const uint16_t* rp = res_row ? a.residual + (int64_t)row * a.ldr + col0 : nullptr;
+    uint32_t w[32];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const uint32_t(&r)[32] = g < 4 ? ra : rb;
+        const int gg = g & 3;
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = unit ? __uint_as_float(r[8 * gg + j]) : __uint_as_float(r[8 * gg + j]) * al;
+        if (res_row && col0 + 8 * g < a.n_valid) {
+            const uint4 r4 = *reinterpret_cast<const uint4*>(rp + 8 * g);
+            const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] += __uint_as_float(rw[j] << 16);
+                f[2 * j + 1] += __uint_as_float(rw[j] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[4 * g + j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
+    }
+    const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
+    const uint32_t swz = (uint32_t)(lane & 7);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        st_shared_v4(dst + ((((uint32_t)g) ^ swz) << 4), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+    epi_release(st, lane, map, EPI_BF16, col0, row0, 0);
+}
+
 // ------------------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -603,6 +644,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             auto chunk_c = [&](int i) { return (i & ((1 << per_h_log) - 1)) * 32; };
             uint32_t ra[32], rb[32];
             __syncwarp();
+            if (ea.epi == EPI_BF16) {
+                // chunk pairs (the N tile is 128 or 256 wide, so pairs never straddle a block)
+                for (int i = 0; i < n_chunks; i += 2) {
+                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i) * pr.bn + chunk_c(i)), ra);
+                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
+                    ptx::tmem_ld_wait(ra);
+                    ptx::tmem_ld_wait(rb);
+                    epi_pair_bf16(ea, omap, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, rb, est, lane);
+                }
+            } else {
             ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * pr.bn + chunk_c(0)), ra);
             ptx::tmem_ld_wait(ra);
             for (int i = 0; i < n_chunks; i += 2) {
@@ -613,6 +664,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * pr.bn + chunk_c(i + 2)), ra);
                 epi_chunk(ea, omap, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est, lane);
                 if (i + 2 < n_chunks) ptx::tmem_ld_wait(ra);
+            }
             }
             ptx::tc_fence_before();
             if (leader) ptx::mbar_arrive(acc_empty_dst);
