@@ -118,8 +118,10 @@ int nf4_dequant(const nf4_view* W, uint16_t* out, void* stream);
  * W is frozen, only the LoRA factors train.  With s = scale (alpha / r):
  *   forward : T = bf16(X A^T);  Y = bf16(X W^T + s T B^T [+ residual])
  *   backward: dT = bf16(s dY B); dB = s dY^T T; dA = dT^T X; dX = dY W + dT A   (no dW)
- * fp32 accumulation on the tensor cores; every reduction has a fixed order (no atomics),
- * so repeated calls give identical bits.  s is applied exactly when it is a power of two.
+ * fp32 accumulation on the tensor cores; every reduction has a fixed order (split-K
+ * partials are summed in split order; accumulate_dX adds each element exactly once, so the
+ * order of those additions never matters), so repeated calls give identical bits.  s is
+ * applied exactly when it is a power of two.
  * Shapes: X [M x k_in], A [r x k_in], B [n_out x r], dY/Y/residual [M x n_out], T [M x r];
  * dX [M x k_in] fp32, dA [r x k_in] fp32, dB [n_out x r] fp32 (overwritten).
  * Limits: k_in % 64 == 0, n_out % 8 == 0, r in {8, 16, 24, ..., 64}, M >= 1.
