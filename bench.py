@@ -1,7 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of the streamed 32-layer NF4-LoRA forward + backward step on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload stream512|stream16k]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload stream512|stream16k|pref1024]
+                    [--recompute] [--resident] [--layers L] [--tokens M] [--no-cpu-baseline]
     python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
 
 One step = layer_stack_step over 32 synthetic Llama-3.1-8B-shaped layers: the forward sweep,
