@@ -178,6 +178,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(pg, value, device):
+    """The largest of every rank's value (each rank's time of the same number of steps), or
+    the value itself on a single rank."""
+    if pg is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, tokens_per_rank, ms_per_step):
+    """Tokens per second of the whole job: every rank runs its own replica of the workload
+    (weak scaling), timed by the slowest rank."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def run_reference(args, world, rank):
     """The oracle arm: the same workload's step, timed on the host cores (rank 0 only)."""
     if rank != 0:
@@ -326,13 +343,9 @@ def main(argv=None):
     lsn.profile_enable(False)
     prof = lsn.profile_read(reset=True)
     lsn.device_check(compute)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(pg, ev0.elapsed_time(ev1) / args.steps, dev)
     pstats = pool.stats()
-    value = world * M / (ms * 1e-3)
+    value = whole_job_rate(world, M, ms)
 
     # ------------------------------------------------------------------- end to end
     e2e_steps = args.e2e_steps or max(3, args.steps // 2)
@@ -345,11 +358,7 @@ def main(argv=None):
         with torch.cuda.stream(compute):
             loss_host.copy_(loss, non_blocking=True)
     torch.cuda.synchronize(dev)
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(pg, (time.perf_counter() - t0) * 1e3 / e2e_steps, dev)
     streamed_bytes = 0 if resident is not None else 2 * L * desc.image_bytes
 
     if rank != 0:
