@@ -311,7 +311,7 @@ __device__ __forceinline__ void epi_release(EpiStage& st, int lane, const CUtens
         const uint32_t src = st.base + st.buf * kEpiStageBytes;
         if (mode == EPI_PARTIAL) ptx::tma_store_3d(map, src, x, y, z);
         else if (mode == EPI_F32_ACC) ptx::tma_reduce_add_2d(map, src, x, y);
-        else ptx::tma_store_2d(map, src, x, y);
+        else ptx::tma_store_2d_hint(map, src, x, y, ptx::policy_evict_first());   // not read again here
         ptx::bulk_commit();
     }
     __syncwarp();
@@ -497,6 +497,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // A rows are read again by the later N tiles of their raster group: keep them in
+            // L2 ahead of the streamed weights and outputs
+            const uint64_t pol_keep = ptx::policy_evict_last();
             SeqPos s;
             seq_begin(p, s, rank);
             uint32_t n_steps = 0;
@@ -515,11 +518,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 ptx::mbar_arrive_expect_tx(bar, bytes);
                 const int ak = sg.a_k0 + s.kk * kBK;
                 if (pr.a_major == A_KMAJOR) {
-                    ptx::tma_load_2d(a_dst, &p.maps[sg.a_map], ak, s.ti.m0, bar);
+                    ptx::tma_load_2d_hint(a_dst, &p.maps[sg.a_map], ak, s.ti.m0, bar, pol_keep);
                 } else {
 #pragma unroll
                     for (int q = 0; q < kBM / 64; ++q)
-                        ptx::tma_load_2d(a_dst + q * 8192, &p.maps[sg.a_map], s.ti.m0 + 64 * q, ak, bar);
+                        ptx::tma_load_2d_hint(a_dst + q * 8192, &p.maps[sg.a_map], s.ti.m0 + 64 * q, ak, bar,
+                                              pol_keep);
                 }
                 const int bk = sg.b_k0 + s.kk * kBK;
                 const int nb = sg.b_n0 + s.ti.n0 + (int)rank * half;
