@@ -1,0 +1,79 @@
+"""CPU-only checks of the C ABI's argument validation: calls with bad shapes, ranks,
+alignments or workspaces are refused with the documented status before any device work,
+and every refusal leaves a message in lsn_last_error().  The pointers are never
+dereferenced, so fake (aligned or misaligned) addresses serve."""
+import ctypes as C
+
+import pytest
+
+import layer_streamed_nf4_quant_b300 as lsn
+from layer_streamed_nf4_quant_b300._lib import nf4_view
+
+ALIGNED = 0x10000      # never dereferenced: validation fails before any device work
+MISALIGNED = 0x10008
+
+
+def _view(n_out, k_in, base=ALIGNED):
+    return nf4_view(C.c_void_p(base), n_out, k_in)
+
+
+def _fwd(view, M=64, r=8, X=ALIGNED, A=ALIGNED, B=ALIGNED, Y=ALIGNED, T=ALIGNED, ws=ALIGNED, ws_bytes=1 << 30):
+    P = C.c_void_p
+    return lsn.lib.lora_nf4_fwd(C.byref(view), P(X), M, P(A), P(B), r, 2.0, None, P(Y), P(T), P(ws), ws_bytes, None)
+
+
+def _bwd(view, M=64, r=8, dX=ALIGNED, ws=ALIGNED, ws_bytes=1 << 30):
+    P = C.c_void_p
+    return lsn.lib.lora_nf4_bwd(C.byref(view), P(ALIGNED), P(ALIGNED), P(ALIGNED), M, P(ALIGNED), P(ALIGNED), r, 2.0,
+                                P(dX), 0, P(ALIGNED), P(ALIGNED), P(ws), ws_bytes, None)
+
+
+def _msg():
+    return lsn.lib.lsn_last_error().decode()
+
+
+@pytest.mark.parametrize("n_out,k_in,r,M", [
+    (128, 100, 8, 64),      # k_in not a multiple of 64
+    (100, 128, 8, 64),      # n_out not a multiple of 8
+    (128, 128, 4, 64),      # r below 8
+    (128, 128, 12, 64),     # r not a multiple of 8
+    (128, 128, 72, 64),     # r above 64
+    (128, 128, 8, 0),       # no rows
+])
+def test_bad_shapes_are_refused(n_out, k_in, r, M):
+    assert _fwd(_view(n_out, k_in), M=M, r=r) == lsn.LSN_EINVAL
+    assert _msg()
+    assert _bwd(_view(n_out, k_in), M=M, r=r) == lsn.LSN_EINVAL
+
+
+def test_misaligned_pointers_are_refused():
+    assert _fwd(_view(128, 128, base=MISALIGNED)) == lsn.LSN_EINVAL
+    assert "aligned" in _msg()
+    assert _fwd(_view(128, 128), X=MISALIGNED) == lsn.LSN_EINVAL
+    assert _fwd(_view(128, 128), Y=MISALIGNED) == lsn.LSN_EINVAL
+    assert _bwd(_view(128, 128), dX=MISALIGNED) == lsn.LSN_EINVAL
+
+
+def test_null_arguments_are_refused():
+    P = C.c_void_p
+    v = _view(128, 128)
+    assert lsn.lib.lora_nf4_fwd(None, P(ALIGNED), 64, P(ALIGNED), P(ALIGNED), 8, 2.0, None, P(ALIGNED), P(ALIGNED),
+                                P(ALIGNED), 1 << 20, None) == lsn.LSN_EINVAL
+    assert _fwd(v, Y=0) == lsn.LSN_EINVAL
+    assert lsn.lib.nf4_dequant(None, P(ALIGNED), None) == lsn.LSN_EINVAL
+
+
+def test_small_workspace_is_refused_with_enomem():
+    # a shape whose forward needs split-K partials: the workspace query says how much
+    M, n_out, k_in, r = 256, 256, 8192, 64
+    need = lsn.lib.lora_nf4_workspace_bytes(M, n_out, k_in, r)
+    assert need > 256
+    assert _bwd(_view(n_out, k_in), M=M, r=r, ws_bytes=64) == lsn.LSN_ENOMEM
+    assert "workspace" in _msg()
+
+
+def test_workspace_query_rejects_bad_shapes():
+    assert lsn.lib.lora_nf4_workspace_bytes(0, 128, 128, 8) == 0
+    assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 32, 8) == 0
+    assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 128, 4) == 0
+    assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 128, 8) > 0
