@@ -51,7 +51,9 @@ int lsn_abi_version(void);
 /* Reads and clears the device error word of the current device after synchronising
  * `stream` (NULL: the legacy default stream).  Returns LSN_OK, LSN_ETIMEOUT (a kernel's
  * bounded wait ran out) or LSN_ECORRUPT (layer tag mismatch); LSN_ECUDA if the
- * synchronisation itself failed.  `detail` (nullable, host) receives the raw word. */
+ * synchronisation itself failed.  `detail` (nullable, host) receives the raw word.  The
+ * error word of lora_nf4_fwd_static_scratch (if that entry point has run on this device) is
+ * read and cleared as well, so a timeout of any call is reported here. */
 int lsn_check(void* stream, uint32_t* detail);
 
 /* Launch accounting and opt-in kernel timing (process-wide).
@@ -117,6 +119,11 @@ int nf4_dequant(const nf4_view* W, uint16_t* out, void* stream);
  * [P1] "How Soup's layer streaming actually works", step 1 "The base model is frozen":
  * W is frozen, only the LoRA factors train.  With s = scale (alpha / r):
  *   forward : T = bf16(X A^T);  Y = bf16(X W^T + s T B^T [+ residual])
+ *             (A == B == NULL in lora_nf4_fwd: the adapter is disabled, Y = bf16(X W^T
+ *             [+ residual]) and T_out is not written and may be NULL.  The LoRA k-steps
+ *             are appended to the last split-K slice, so the base contraction is summed in
+ *             the same order with or without the adapter: B = 0 gives the adapter-disabled
+ *             Y bit for bit.)
  *   backward: dT = bf16(s dY B); dB = s dY^T T; dA = dT^T X; dX = dY W + dT A   (no dW)
  * fp32 accumulation on the tensor cores; every reduction has a fixed order (split-K
  * partials are summed in split order; accumulate_dX adds each element exactly once, so the
@@ -144,8 +151,12 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M,
  * cudaGetSymbolAddress and clears the word (synchronously), so make that first call before
  * any stream capture.  All calls on a device share the buffer: calls whose kernels overlap on
  * the GPU race.  A shape whose split-K partials exceed 16 MiB is rejected with LSN_ENOMEM.
+ * A, B and T_out are required here (no adapter-disabled mode); every pointer is checked for
+ * NULL and 16-byte alignment exactly as in lora_nf4_fwd (LSN_EINVAL).
  * device_status (host, nullable): if given, the call synchronises `stream`, stores the word
- * there, clears it and returns LSN_ETIMEOUT if a device wait ran out. */
+ * there, clears it and returns LSN_ETIMEOUT if a device wait ran out.  A timeout of an earlier
+ * call made without device_status that lsn_check() has not collected yet is reported by that
+ * read too. */
 int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X, int64_t M,
                                 const uint16_t* A, const uint16_t* B, int r, float scale,
                                 const uint16_t* residual /* nullable */, uint16_t* Y,
@@ -305,6 +316,12 @@ typedef struct {
     /* nullable: when set, each layer's AdamW update runs in the reverse sweep right after
      * that layer's dA/dB are written (they are still written to grads). */
     const lsn_adamw_state* adamw;
+    /* nullable, device bf16 [n_layers][M][d_model]: slice l receives x_{l+1}, the output of
+     * layer l, at the end of the forward sweep (for per-layer checks). */
+    uint16_t* x_layers_out;
+    /* nullable, device fp32 [n_layers][M][d_model]: slice l receives dloss/dx_l, the gradient
+     * with respect to layer l's input, right after layer l's backward. */
+    float* dx_layers_out;
 } lsn_step_opts;
 
 size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts* opts);

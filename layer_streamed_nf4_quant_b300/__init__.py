@@ -81,12 +81,15 @@ def lora_workspace(M: int, n_out: int, k_in: int, r: int, device="cuda"):
 
 
 def lora_nf4_fwd(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, T=None, ws=None, stream=None):
-    """Y = bf16(X W^T + s T B^T [+ residual]), T = bf16(X A^T).  Returns (Y, T)."""
+    """Y = bf16(X W^T + s T B^T [+ residual]), T = bf16(X A^T).  Returns (Y, T).
+
+    A = B = None disables the adapter: Y = bf16(X W^T [+ residual]) and T is None."""
     torch = _torch()
     M = X.shape[0]
+    adapter = A is not None or B is not None
     if Y is None:
         Y = torch.empty((M, n_out), dtype=torch.bfloat16, device=X.device)
-    if T is None:
+    if T is None and adapter:
         T = torch.empty((M, r), dtype=torch.bfloat16, device=X.device)
     if ws is None:
         ws = lora_workspace(M, n_out, k_in, r, X.device)
@@ -297,16 +300,20 @@ class AdamW:
 
 def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
                      resident_store=None, x_out=None, dx0=None, stream=None, recompute: bool = False,
-                     reference_pass: bool = False, x_ref_out=None, adamw: "AdamW | None" = None):
+                     reference_pass: bool = False, x_ref_out=None, adamw: "AdamW | None" = None,
+                     x_layers_out=None, dx_layers_out=None):
     """One forward + loss + backward pass over the stack (streamed through `pool`, or resident).
 
     recompute: keep only x_l per layer and recompute the rest in the reverse sweep.
     reference_pass: also run the adapter-disabled forward on the same streamed slots and write
-    it to x_ref_out."""
+    it to x_ref_out.
+    x_layers_out: bf16 [L, M, d_model] receives every layer's output x_{l+1}.
+    dx_layers_out: fp32 [L, M, d_model] receives the gradient w.r.t. every layer's input x_l."""
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
-    if not (recompute or reference_pass or x_ref_out is not None or adamw is not None):
+    if not (recompute or reference_pass or x_ref_out is not None or adamw is not None or
+            x_layers_out is not None or dx_layers_out is not None):
         check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                    _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws),
                                    ws.numel(), _stream(stream)))
@@ -315,6 +322,8 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
     if adamw is not None:
         st = adamw.state()
         o.adamw = C.pointer(st)
+    o.x_layers_out = None if x_layers_out is None else x_layers_out.data_ptr()
+    o.dx_layers_out = None if dx_layers_out is None else dx_layers_out.data_ptr()
     check(lib.layer_stack_step_ex(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                   C.byref(o), _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(x_ref_out),
                                   _p(dx0), _p(ws), ws.numel(), _stream(stream)))

@@ -52,7 +52,8 @@ class lsn_adamw_state(C.Structure):
 
 class lsn_step_opts(C.Structure):
     _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6),
-                ("adamw", C.POINTER(lsn_adamw_state))]
+                ("adamw", C.POINTER(lsn_adamw_state)), ("x_layers_out", C.c_void_p),
+                ("dx_layers_out", C.c_void_p)]
 
 
 class lsn_profile(C.Structure):

@@ -338,7 +338,7 @@ extern "C" {
 
 const char* lsn_last_error(void) { return g_err; }
 
-int lsn_abi_version(void) { return 1; }
+int lsn_abi_version(void) { return 2; }
 
 uint64_t lsn_launch_count(void) { return g_launches.load(); }
 
@@ -381,9 +381,14 @@ int lsn_check(void* stream, uint32_t* detail) {
     if (!w) return LSN_ECUDA;
     uint32_t v = 0;
     LSN_CUDA_TRY(cudaMemcpy(&v, w, 4, cudaMemcpyDeviceToHost));
+    if (v) LSN_CUDA_TRY(cudaMemset(w, 0, 4));
+    // the static-scratch entry point keeps its own word: collect it here as well
+    uint32_t vs = 0;
+    int rc = static_error_take(&vs);
+    if (rc) return rc;
+    if (!v) v = vs;
     if (detail) *detail = v;
     if (v == 0) return LSN_OK;
-    LSN_CUDA_TRY(cudaMemset(w, 0, 4));
     uint32_t kind = v >> 24;
     if (kind == kDevErrTag)
         return fail(LSN_ECORRUPT, "layer image tag mismatch (expected layer %u)", v & 0xFFFFFFu);

@@ -209,7 +209,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         int mt = g.map(b.tcat[l], M, 5 * r, 5 * r, kBM);
         int tiles = 0;
         for (int p = 0; p < 5; ++p) tiles += tiles_of(M, d.np[p], 256);
-        const int sp = choose_splits(tiles, D / kBK + 1);
+        const int sp = choose_splits(tiles, D / kBK);
         for (int p = 0; p < 5; ++p) {
             int v = g.nf4(c.mat(img, p), d.np[p], D);
             g.problem(M, d.np[p], 256, A_KMAJOR, EPI_BF16, b.y[l] ? b.y[l] + d.coff[p] : nullptr, d.Ncat, 1.0f,
@@ -243,7 +243,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         int vo = g.nf4(c.mat(img, kO), D, D);
         int vd = g.nf4(c.mat(img, kDown), D, d.F);
         g.problem(M, D, 256, A_KMAJOR, EPI_BF16, b.x[l + 1], D, 1.0f, D,
-                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK + 2), b.x[l], D);
+                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK), b.x[l], D);
         g.seg(mq, 0, B_NF4_K, vo, 0, 0, D);
         g.seg(ma, 0, B_NF4_K, vd, 0, 0, d.F);
         g.seg_scaled(mt, 0, c.B(lora, kO), r, D, r, d.s);
@@ -328,7 +328,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         int vd = g.nf4(c.mat(img, kDown), D, F);
         const int tiles = 3 * tiles_of(D, r, 64) + tiles_of(F, r, 64) + tiles_of(M, D, 256) + tiles_of(M, F, 256);
         const int ws = choose_splits(tiles, ceil_div(M, kBK));
-        const int xs = choose_splits(tiles, D / kBK + 1);
+        const int xs = choose_splits(tiles, D / kBK);
         g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kO), r, d.s, r, ws);
         g.seg(mdx_mn, 0, B_TMA_MN, mtod_mn, 0, 0, M);
         g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kDown), r, d.s, r, ws);
@@ -339,10 +339,10 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         g.seg(ma_mn, 0, B_TMA_MN, mdtod_mn, 0, r, M);
         g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dqa, D + F, 1.0f, D, xs);
         g.seg(mdx, 0, B_NF4_MN, vo, 0, 0, D);
-        g.seg(mdtod, 0, B_TMA_MN, mao, 0, 0, r);
+        g.seg(mdtod, 0, B_TMA_MN, mao, 0, 0, r, true);
         g.problem(M, F, 256, A_KMAJOR, EPI_F32, b.dqa ? b.dqa + D : nullptr, D + F, 1.0f, F, xs);
         g.seg(mdx, 0, B_NF4_MN, vd, 0, 0, D);
-        g.seg(mdtod, r, B_TMA_MN, mad, 0, 0, r);
+        g.seg(mdtod, r, B_TMA_MN, mad, 0, 0, r, true);
         RC(c.run(g));
     }
     if (!c.dry)
@@ -380,14 +380,14 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
             g.problem(D, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, p), D, 1.0f, r, ws);
             g.seg(mh_mn, 0, B_TMA_MN, mdtcat_mn, 0, p * r, M);
         }
-        int ksteps = 1;
+        int ksteps = 0;
         for (int p = 0; p < 5; ++p) ksteps += ceil_div(d.np[p], kBK);
         g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dh, D, 1.0f, D, choose_splits(tiles, ksteps));
         for (int p = 0; p < 5; ++p) {
             int v = g.nf4(c.mat(img, p), d.np[p], D);
             g.seg(mdy, d.coff[p], B_NF4_MN, v, 0, 0, d.np[p]);
         }
-        g.seg(mdtcat, 0, B_TMA_MN, macat, 0, 0, 5 * r);
+        g.seg(mdtcat, 0, B_TMA_MN, macat, 0, 0, 5 * r, true);
         RC(c.run(g));
     }
     if (!c.dry) RC(launch_rmsnorm_bwd(b.x[l], b.rstd[l], b.dh, b.dx, b.dx_bf, M, D, c.s));
@@ -496,6 +496,11 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         }
         if (pool) RC(stream_pool_release(pool, l, stream));
     }
+    const size_t act = (size_t)c.d.M * c.d.D;
+    if (c.o.x_layers_out)
+        for (int l = 0; l < L; ++l)
+            LSN_CUDA_TRY(cudaMemcpyAsync(c.o.x_layers_out + (size_t)l * act, c.b.x[l + 1], act * 2,
+                                         cudaMemcpyDeviceToDevice, c.s));
     RC(launch_loss(c.b.x[L], c.d.M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart, loss_out,
                    c.s));
     // reverse sweep, re-streaming every layer (and recomputing its activations if asked)
@@ -506,6 +511,9 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         RC(image(l, &img));
         if (c.o.recompute) RC(fwd_layer(c, l, img, lora[l], true));
         RC(bwd_layer(c, l, img, lora[l], grads[l]));
+        if (c.o.dx_layers_out)
+            LSN_CUDA_TRY(cudaMemcpyAsync(c.o.dx_layers_out + (size_t)l * act, c.b.dx, act * 4,
+                                         cudaMemcpyDeviceToDevice, c.s));
         if (c.o.adamw) {
             const lsn_adamw_state* st = c.o.adamw;
             RC(launch_adamw(st->hp, st->master[l], st->lora_out[l], grads[l], st->m[l], st->v[l],

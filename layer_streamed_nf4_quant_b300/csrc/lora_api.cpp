@@ -26,11 +26,18 @@ struct LinearShape {
 struct FwdSplits { int t, y; };
 struct BwdSplits { int dt, db, da, dx; };
 
+// The LoRA k-steps of the Y launch are a tail (they go to the last split), so the splits
+// divide the base contraction only: the adapter-disabled launch splits it the same way.
 static FwdSplits fwd_splits(const LinearShape& s) {
     FwdSplits f;
     f.t = choose_splits(tiles_of(s.M, s.r, 64), ksteps_of(s.K));
-    f.y = choose_splits(tiles_of(s.M, s.N, bn_for(s.N)), ksteps_of(s.K) + 1);
+    f.y = choose_splits(tiles_of(s.M, s.N, bn_for(s.N)), ksteps_of(s.K));
     return f;
+}
+
+LinearFwdSplits linear_fwd_splits(int64_t M, int64_t n_out, int64_t k_in, int r) {
+    const FwdSplits f = fwd_splits(LinearShape{M, n_out, k_in, r});
+    return LinearFwdSplits{f.t, f.y};
 }
 
 static BwdSplits bwd_splits(const LinearShape& s) {
@@ -39,7 +46,7 @@ static BwdSplits bwd_splits(const LinearShape& s) {
     const int tiles2 = tiles_of(s.N, s.r, 64) + tiles_of(s.K, s.r, 64) + tiles_of(s.M, s.K, bn_for(s.K));
     b.db = choose_splits(tiles2, ksteps_of(s.M));
     b.da = b.db;
-    b.dx = choose_splits(tiles2, ksteps_of(s.N) + 1);
+    b.dx = choose_splits(tiles2, ksteps_of(s.N));
     return b;
 }
 
@@ -65,6 +72,21 @@ static int check_linear(const nf4_view* W, int64_t M, int r, const void* X) {
     if (r < 8 || r > 64 || r % 8) return fail(LSN_EINVAL, "lora: r must be 8..64, a multiple of 8");
     if (M < 1 || M > (1 << 30)) return fail(LSN_EINVAL, "lora: bad M");
     if (!al16(W->base) || !al16(X)) return fail(LSN_EINVAL, "lora: pointers must be 16-byte aligned");
+    return LSN_OK;
+}
+
+int check_linear_fwd(const char* who, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,
+                     const uint16_t* B, int r, const uint16_t* residual, const uint16_t* Y,
+                     const uint16_t* T_out, bool adapter) {
+    if (!W || !W->base || !X || !Y || (adapter && (!A || !B || !T_out)))
+        return fail(LSN_EINVAL, "%s: NULL argument", who);
+    if (W->k_in < 64 || W->k_in % 64 || W->n_out < 8 || W->n_out % 8)
+        return fail(LSN_EINVAL, "%s: need k_in %% 64 == 0 and n_out %% 8 == 0", who);
+    if (r < 8 || r > 64 || r % 8) return fail(LSN_EINVAL, "%s: r must be 8..64, a multiple of 8", who);
+    if (M < 1 || M > (1 << 30)) return fail(LSN_EINVAL, "%s: bad M", who);
+    if (!al16(W->base) || !al16(X) || !al16(Y) || (residual && !al16(residual)) ||
+        (adapter && (!al16(A) || !al16(B) || !al16(T_out))))
+        return fail(LSN_EINVAL, "%s: pointers must be 16-byte aligned", who);
     return LSN_OK;
 }
 
@@ -100,11 +122,10 @@ int nf4_dequant(const nf4_view* W, uint16_t* out, void* stream) {
 int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A, const uint16_t* B,
                  int r, float scale, const uint16_t* residual, uint16_t* Y, uint16_t* T_out, void* ws,
                  size_t ws_bytes, void* stream) {
-    int rc = check_linear(W, M, r, X);
+    // A == B == NULL: the adapter is disabled; Y is the frozen linear alone
+    const bool adapter = A || B;
+    int rc = check_linear_fwd("lora_nf4_fwd", W, X, M, A, B, r, residual, Y, T_out, adapter);
     if (rc) return rc;
-    if (!A || !B || !Y || !T_out) return fail(LSN_EINVAL, "lora_nf4_fwd: NULL argument");
-    if (!al16(A) || !al16(B) || !al16(Y) || !al16(T_out) || (residual && !al16(residual)))
-        return fail(LSN_EINVAL, "lora_nf4_fwd: pointers must be 16-byte aligned");
     const LinearShape s{M, W->n_out, W->k_in, r};
     if (ws_bytes < fwd_ws(s) || (fwd_ws(s) && !ws))
         return fail(LSN_ENOMEM, "lora_nf4_fwd: workspace %zu < %zu", ws_bytes, fwd_ws(s));
@@ -113,7 +134,7 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t
     const int K = (int)s.K, N = (int)s.N, m = (int)M;
 
     // T = bf16(X A^T)
-    {
+    if (adapter) {
         GemmPlan g;
         int mx = g.map(X, M, K, K, kBM);
         int ma = g.map(A, r, K, K, 64);
@@ -127,11 +148,10 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t
         uint8_t* wsb = static_cast<uint8_t*>(ws) + partial_bytes(f.t, s.M, s.r);
         GemmPlan g;
         int mx = g.map(X, M, K, K, kBM);
-        int mt = g.map(T_out, M, r, r, kBM);
         int wv = g.nf4(W->base, N, K);
         g.problem(m, N, bn_for(N), A_KMAJOR, EPI_BF16, Y, N, 1.0f, N, f.y, residual, N);
         g.seg(mx, 0, B_NF4_K, wv, 0, 0, K);
-        g.seg_scaled(mt, 0, B, r, N, r, scale);
+        if (adapter) g.seg_scaled(g.map(T_out, M, r, r, kBM), 0, B, r, N, r, scale);
         rc = g.launch(st, reinterpret_cast<float*>(wsb), ws_bytes - (wsb - static_cast<uint8_t*>(ws)));
         if (rc) return rc;
     }
@@ -185,7 +205,7 @@ int lora_nf4_bwd(const nf4_view* W, const uint16_t* X, const uint16_t* T, const 
             int wv = g.nf4(W->base, N, K);
             g.problem(m, K, bn_for(K), A_KMAJOR, accumulate_dX ? EPI_F32_ACC : EPI_F32, dX, K, 1.0f, K, b.dx);
             g.seg(my, 0, B_NF4_MN, wv, 0, 0, N);
-            g.seg(mdt, 0, B_TMA_MN, ma_mn, 0, 0, r);
+            g.seg(mdt, 0, B_TMA_MN, ma_mn, 0, 0, r, true);
         }
         rc = g.launch(st, reinterpret_cast<float*>(wsb + off), ws_bytes - off);
         if (rc) return rc;

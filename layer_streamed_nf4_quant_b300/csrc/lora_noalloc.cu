@@ -16,7 +16,8 @@
 // a stream capture.  All calls on a device share the same scratch: calls whose kernels
 // overlap on the GPU (for example on two streams without ordering) race and must not be
 // made.  The partial sums are fully written before they are read, so only the error word
-// has to start at zero.
+// has to start at zero.  A device-wait timeout of a call made without device_status stays in
+// the word until lsn_check() or the next call with device_status reads and clears it.
 #include <mutex>
 
 #include "lsn_internal.h"
@@ -66,6 +67,23 @@ inline size_t partial_bytes(int splits, int64_t m, int64_t n) {
 }
 
 }  // namespace
+
+int static_error_take(uint32_t* v) {
+    *v = 0;
+    int dev = 0;
+    LSN_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return LSN_OK;
+    uint32_t* w = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        w = g_static_addr[dev].err;
+    }
+    if (!w) return LSN_OK;   // the entry point has not run on this device
+    LSN_CUDA_TRY(cudaMemcpy(v, w, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    if (*v) LSN_CUDA_TRY(cudaMemset(w, 0, sizeof(uint32_t)));
+    return LSN_OK;
+}
+
 }  // namespace lsn
 
 using namespace lsn;
@@ -74,18 +92,14 @@ extern "C" int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X,
                                            const uint16_t* B, int r, float scale, const uint16_t* residual,
                                            uint16_t* Y, uint16_t* T_out, uint32_t* device_status,
                                            void* stream) {
-    if (!W || !W->base || !X || !A || !B || !Y || !T_out)
-        return fail(LSN_EINVAL, "lora_nf4_fwd_static_scratch: NULL argument");
-    if (W->k_in < 64 || W->k_in % 64 || W->n_out < 8 || W->n_out % 8 || r < 8 || r > 64 || r % 8 || M < 1 ||
-        M > (1 << 30))
-        return fail(LSN_EINVAL, "lora_nf4_fwd_static_scratch: need k_in %% 64 == 0, n_out %% 8 == 0, r in 8..64");
+    // the same checks (shapes, NULLs, 16-byte alignment of every pointer) as lora_nf4_fwd
+    int rc = check_linear_fwd("lora_nf4_fwd_static_scratch", W, X, M, A, B, r, residual, Y, T_out, true);
+    if (rc) return rc;
     const int K = (int)W->k_in, N = (int)W->n_out, m = (int)M;
     // the same split decisions as lora_nf4_fwd, so both give the same bits
     const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-    const int tiles_t = pair_tiles(M, r, 64);
-    const int tiles_y = pair_tiles(M, N, bn);
-    const int st = choose_splits(tiles_t, (K + kBK - 1) / kBK);
-    const int sy = choose_splits(tiles_y, (K + kBK - 1) / kBK + 1);
+    const LinearFwdSplits sp = linear_fwd_splits(M, N, K, r);
+    const int st = sp.t, sy = sp.y;
     const size_t need_t = partial_bytes(st, M, r), need_y = partial_bytes(sy, M, N);
     const size_t need = need_t > need_y ? need_t : need_y;
     if (need > kStaticScratchBytes)
@@ -94,7 +108,7 @@ extern "C" int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X,
                     "scratch holds %zu bytes (use lora_nf4_fwd with a caller workspace)",
                     need, kStaticScratchBytes);
     StaticAddrs sa;
-    int rc = static_addresses(&sa);
+    rc = static_addresses(&sa);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* scratch = static_cast<float*>(sa.scratch);

@@ -28,6 +28,21 @@ enum DeviceErrorKind : uint32_t {
     kDevErrTag = 2u,       // layer image tag mismatch (detail: expected layer)
 };
 
+// Split counts of the single-linear forward (the T launch and the Y launch).  Shared by
+// lora_nf4_fwd and lora_nf4_fwd_static_scratch, so the two give the same bits.
+struct LinearFwdSplits {
+    int t, y;
+};
+LinearFwdSplits linear_fwd_splits(int64_t M, int64_t n_out, int64_t k_in, int r);
+// Argument checks of the single-linear forward entry points (shapes, NULLs, 16-byte
+// alignment of every operand and output).  adapter == false: A, B and T_out are not used.
+int check_linear_fwd(const char* who, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,
+                     const uint16_t* B, int r, const uint16_t* residual, const uint16_t* Y,
+                     const uint16_t* T_out, bool adapter);
+// Reads and clears the static-scratch entry point's error word of the current device
+// (0 if that entry point has not been called on it).
+int static_error_take(uint32_t* v);
+
 // Launch accounting: every kernel launch site calls note_launch().
 void note_launch();
 // GEMM profiling hooks (no-ops unless lsn_profile_enable(1) was called).

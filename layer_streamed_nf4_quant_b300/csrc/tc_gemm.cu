@@ -167,8 +167,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, uint
     ti.m0 = (2 * mt + (int)rank) * kBM;
     ti.n0 = nt * pr.bn;
     ti.split = s;
-    ti.ks_begin = (int)((int64_t)pr.ksteps * s / pr.splits);
-    ti.ks_end = (int)((int64_t)pr.ksteps * (s + 1) / pr.splits);
+    const int64_t kb = pr.ksteps_split;
+    ti.ks_begin = (int)(kb * s / pr.splits);
+    ti.ks_end = s + 1 == pr.splits ? pr.ksteps : (int)(kb * (s + 1) / pr.splits);
     ti.half0 = ti.m0 < pr.m;
     ti.half1 = ti.m0 + 128 < pr.m;
     return ti;
@@ -1030,10 +1031,12 @@ int GemmPlan::problem(int m, int n, int bn, int a_major, int epi, void* out, int
     return p_.n_probs++;
 }
 
-int GemmPlan::seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len) {
+int GemmPlan::seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len, bool tail) {
     if (status_) return -1;
     if (p_.n_probs == 0 || n_segs_ >= kMaxSegs || k_len < 1 || (a_k0 % 8) || a_map < 0 || a_map >= n_maps_)
         return status_ = fail(LSN_EINVAL, "gemm: bad segment");
+    if (!tail && p_.probs[p_.n_probs - 1].ksteps != p_.probs[p_.n_probs - 1].ksteps_split)
+        return status_ = fail(LSN_EINVAL, "gemm: a base segment after a tail segment");
     if ((b_src == B_TMA_K || b_src == B_TMA_MN) && (b_idx < 0 || b_idx >= n_maps_))
         return status_ = fail(LSN_EINVAL, "gemm: bad B map");
     {
@@ -1061,6 +1064,7 @@ int GemmPlan::seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0,
     Problem& pr = p_.probs[p_.n_probs - 1];
     pr.seg_count++;
     pr.ksteps += s.ksteps;
+    if (!tail) pr.ksteps_split += s.ksteps;
     return n_segs_++;
 }
 
@@ -1070,7 +1074,7 @@ int GemmPlan::seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, i
     if ((!b_ptr && !dry_) || k_len < 8 || k_len > 64 || k_len % 8 || b_ld % 8 ||
         (reinterpret_cast<uintptr_t>(b_ptr) & 15))
         return status_ = fail(LSN_EINVAL, "gemm: bad scaled segment");
-    int s = seg(a_map, a_k0, B_SCALED_K, 0, 0, 0, k_len);
+    int s = seg(a_map, a_k0, B_SCALED_K, 0, 0, 0, k_len, true);
     if (s < 0) return s;
     p_.segs[s].b_ptr = b_ptr;
     p_.segs[s].b_ld = b_ld;
@@ -1083,7 +1087,7 @@ size_t GemmPlan::partial_bytes() const {
     size_t b = 0;
     for (int i = 0; i < p_.n_probs; ++i) {
         const Problem& pr = p_.probs[i];
-        const int splits = pr.splits > pr.ksteps ? pr.ksteps : pr.splits;
+        const int splits = pr.splits > pr.ksteps_split ? pr.ksteps_split : pr.splits;
         if (splits > 1) b += (size_t)splits * pr.m * pr.n * sizeof(float);
     }
     return b;
@@ -1101,7 +1105,7 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     for (int i = 0; i < p_.n_probs; ++i) {
         Problem& pr = p_.probs[i];
         if (pr.seg_count == 0) return status_ = fail(LSN_EINVAL, "gemm: problem without segments");
-        if (pr.splits > pr.ksteps) pr.splits = pr.ksteps;
+        if (pr.splits > pr.ksteps_split) pr.splits = pr.ksteps_split > 0 ? pr.ksteps_split : 1;
         pr.tiles_m = ((pr.m + kBM - 1) / kBM + 1) / 2;   // M-pairs: one per CTA pair
         pr.tiles_n = (pr.n + pr.bn - 1) / pr.bn;
         // raster group: as many M-pairs as keep their A rows (512 x K bf16 each) within

@@ -66,6 +66,8 @@ struct Problem {
     int a_major;
     int seg_begin, seg_count;
     int ksteps;        // total over the segments
+    int ksteps_split;  // k-steps of the leading (non-tail) segments, which the splits divide;
+                       // the tail segments' k-steps all go to the last split
     int splits;
     int tiles_m, tiles_n;
     int raster;        // M-pairs per raster group (set at launch)
@@ -114,7 +116,11 @@ class GemmPlan {
     int problem(int m, int n, int bn, int a_major, int epi, void* out, int64_t ldo, float alpha,
                 int n_valid, int splits = 1, const uint16_t* residual = nullptr,
                 int64_t ldr = 0);
-    int seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len);
+    // tail: a LoRA contraction appended to the base one.  Tail segments follow every
+    // non-tail segment of their problem, and all their k-steps belong to the last split, so
+    // the base k-steps are split exactly as in the same problem without the tail.
+    int seg(int a_map, int a_k0, int b_src, int b_idx, int b_k0, int b_n0, int k_len, bool tail = false);
+    // Always a tail segment.
     int seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, int b_rows, int k_len,
                    float b_scale);
     // Bytes of split-K partial workspace the launch needs (after clamping splits).

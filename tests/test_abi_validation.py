@@ -77,3 +77,32 @@ def test_workspace_query_rejects_bad_shapes():
     assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 32, 8) == 0
     assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 128, 4) == 0
     assert lsn.lib.lora_nf4_workspace_bytes(64, 128, 128, 8) > 0
+
+
+def _fwd_static(view, M=64, r=8, X=ALIGNED, A=ALIGNED, B=ALIGNED, Y=ALIGNED, T=ALIGNED, residual=None):
+    P = C.c_void_p
+    return lsn.lib.lora_nf4_fwd_static_scratch(C.byref(view), P(X), M, P(A), P(B), r, 2.0,
+                                               None if residual is None else P(residual), P(Y), P(T), None, None)
+
+
+def test_static_scratch_checks_alignment_like_the_workspace_entry():
+    """The allocation-free forward refuses every misaligned operand or output that
+    lora_nf4_fwd refuses, instead of handing it to a kernel that stores 16-byte vectors."""
+    v = _view(128, 128)
+    for kw in ({"residual": MISALIGNED}, {"Y": MISALIGNED}, {"T": MISALIGNED}, {"X": MISALIGNED},
+               {"A": MISALIGNED}, {"B": MISALIGNED}):
+        assert _fwd_static(v, **kw) == lsn.LSN_EINVAL, kw
+        assert "aligned" in _msg()
+    assert _fwd_static(_view(128, 128, base=MISALIGNED)) == lsn.LSN_EINVAL
+    assert _fwd_static(v, T=0) == lsn.LSN_EINVAL          # no adapter-disabled mode here
+    assert "NULL" in _msg()
+
+
+def test_adapter_disabled_forward_validation():
+    """lora_nf4_fwd with A = B = NULL is the frozen linear: T may be NULL then, but a
+    half-given adapter (only A or only B) is refused."""
+    v = _view(128, 128)
+    assert _fwd(v, A=0, B=ALIGNED) == lsn.LSN_EINVAL
+    assert _fwd(v, A=ALIGNED, B=0) == lsn.LSN_EINVAL
+    assert _fwd(v, A=0, B=0, T=0, X=MISALIGNED) == lsn.LSN_EINVAL   # still validated
+    assert "aligned" in _msg()

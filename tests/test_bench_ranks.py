@@ -51,3 +51,28 @@ def test_two_gloo_ranks_take_the_slowest_rank_and_count_every_token():
 def test_single_rank_passes_its_own_time():
     assert bench.max_over_ranks(None, 3.5, "cpu") == 3.5
     assert bench.whole_job_rate(1, 512, 130.0) == pytest.approx(512 / 0.13)
+
+
+def test_gpus_flag_starts_one_rank_per_gpu_without_a_launcher():
+    """`bench.py --gpus 2` with no launcher in the environment starts two local ranks through
+    torch.distributed.run (rendezvous on 127.0.0.1); each rank binds the device of its local
+    rank.  --show-ranks stops each rank right after the binding, before any device work."""
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--show-ranks"], capture_output=True,
+                       text=True, timeout=180, env=env)
+    assert r.returncode == 0, r.stderr
+    ranks = sorted((json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")), key=lambda d: d["rank"])
+    assert [d["rank"] for d in ranks] == [0, 1]
+    assert all(d["world"] == 2 for d in ranks)
+    assert [d["device"] for d in ranks] == ["cuda:0", "cuda:1"]
+
+
+def test_launcher_world_must_match_gpus():
+    cmd = bench.launcher_command(4, ["--gpus", "4"], 12345)
+    assert "--nproc-per-node=4" in cmd and "127.0.0.1" in cmd and cmd[-2:] == ["--gpus", "4"]
+    bench.check_world(2, 2)
+    with pytest.raises(SystemExit):
+        bench.check_world(2, 1)

@@ -161,3 +161,32 @@ def test_accumulate_dx_and_zero_A_gives_zero_dB():
     torch.cuda.synchronize()
     # one fp32 addition per element of the same deterministic dX: exactly twice dX1
     assert torch.equal(dX2, 2 * dX1)
+
+
+@pytest.mark.parametrize("M,N,K,r,residual", [(128, 1024, 512, 8, False),    # split-K: 4 slices
+                                              (300, 776, 192, 16, True),
+                                              (513, 320, 1088, 24, False),
+                                              (16, 4096, 4096, 64, True)])   # split-K: 16 slices
+def test_zero_B_bit_identical_to_adapter_disabled_launch(M, N, K, r, residual):
+    """B = 0: every LoRA product is an exact zero, so Y must equal the frozen linear launched
+    without the adapter (A = B = NULL) bit for bit, split-K slices included."""
+    from synth import random_bf16
+    lsn = _lsn()
+    inp = _case(M, N, K, r, seed=3 * M + N)
+    packed = torch.from_numpy(lsn.nf4_pack(inp["W"])).cuda()
+    X, A = _bf16_dev(inp["X"]), _bf16_dev(inp["A"])
+    B0 = torch.zeros((N, r), dtype=torch.bfloat16, device="cuda")
+    res = _bf16_dev(random_bf16((M, N), 7)) if residual else None
+    Y0, T0 = lsn.lora_nf4_fwd(packed, N, K, X, A, B0, r, 16.0 / r, residual=res)
+    Yf, Tf = lsn.lora_nf4_fwd(packed, N, K, X, None, None, r, 16.0 / r, residual=res)
+    torch.cuda.synchronize()
+    assert lsn.device_check() == 0
+    assert Tf is None and torch.count_nonzero(T0) > 0
+    assert torch.equal(Y0.view(torch.int16), Yf.view(torch.int16))
+    # the frozen linear itself against the oracle (the adapter-disabled path is a real path)
+    from oracle import nf4 as onf4
+    Wh = onf4.dequantize(onf4.quantize(inp["W"]))
+    ref = _f64_of_bits(inp["X"]) @ Wh.T
+    if residual:
+        ref = ref + _f64_of_bits(_bits(res))
+    assert _max_rel(_f64_of_bits(_bits(Yf)), ref) <= FWD_TOL

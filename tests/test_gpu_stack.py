@@ -184,6 +184,47 @@ def test_reference_pass_shares_the_stream(small):
     assert np.max(np.abs(got - x_pol)) > 0                   # the adapter does change the output
 
 
+def test_zero_B_stack_bit_identical_to_reference_pass(small):
+    """B = 0 in every layer: the policy stack is the frozen stack, so its output must equal
+    the adapter-disabled reference pass (LoRA steps left out of the GEMMs) bit for bit."""
+    lsn = _lsn()
+    d = small.desc
+    saved = small.lora
+    try:
+        zeroed = []
+        for blob in saved:
+            z = blob.clone()
+            _, B = d.lora_views(z)
+            for p in B:
+                B[p].zero_()
+            zeroed.append(z)
+        small.lora = zeroed
+        out = small.run(reference=True)
+    finally:
+        small.lora = saved
+    assert torch.equal(out["x"].view(torch.int16), out["x_ref"].view(torch.int16))
+
+
+def test_host_wait_timeout_then_recovery(small):
+    """stream_pool_wait with a host timeout: a copy held back by the injected delay makes the
+    bounded poll return LSN_ETIMEOUT; once the copy lands the pool goes on, and a full step
+    through it still gives the resident bits."""
+    lsn = _lsn()
+    base = small.run()
+    pool = small.pool()
+    pool.set_copy_delay_us(300000)
+    pool.prefetch(0)
+    with pytest.raises(lsn.LsnError) as e:
+        pool.wait(0, timeout_ms=5)
+    assert e.value.code == lsn.LSN_ETIMEOUT
+    torch.cuda.synchronize()
+    pool.stats()                                              # the delayed copy has landed
+    pool.release(0)
+    pool.set_copy_delay_us(0)
+    _same(base, small.run(pool))
+    pool.close()
+
+
 def test_pool_misuse_is_reported(small):
     lsn = _lsn()
     pool = small.pool()

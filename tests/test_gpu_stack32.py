@@ -1,0 +1,235 @@
+"""GPU parity of the full 32-layer stack at the workload sizes themselves, against the fp64
+oracle (the oracle quantises and dequantises all 32 layers itself; see _oracle_layers.py).
+
+* batch 1 x 512 tokens, streamed: loss, x_32, dx0 and every layer's dA_p, dB_p end to end,
+  and every layer teacher-forced (the oracle's layer l run on the GPU's own x_l and, in the
+  backward, on the GPU's own dloss/dx_{l+1}), so that error growth over 32 layers and a
+  per-layer mistake are told apart.  "Can You Fine-Tune Llama 3.1 8B on a 4GB GPU? Soup's
+  Layer Streaming Explained", section "The gradient bug also reveals something important
+  about AI benchmarks": the forward output and the LoRA gradients are checked separately.
+* batch 8 x 2048 tokens: the streamed run bit-identical to the resident run, and sampled
+  token rows of x_32 and dx0 against the oracle run on those rows (layers are independent
+  across tokens; the loss normalisation uses the full token count).
+* preference pair, 2 x 512 tokens: the adapter-disabled reference pass on the same streamed
+  slots against the oracle's frozen stack on sampled rows, with no extra layer copies.
+* B = 0 in every layer: the policy stack equals the reference pass bit for bit.
+
+Bars: forward max|y - y_ref| / max|y_ref| <= 2e-2; gradients ||g - g_ref||_F / ||g_ref||_F
+<= 1e-2; streamed against resident bit-identical.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FWD_TOL = 2e-2
+GRAD_TOL = 1e-2
+L = 32
+
+
+def _lsn():
+    import layer_streamed_nf4_quant_b300 as lsn
+    return lsn
+
+
+def _f64_bits(t):
+    from oracle.nf4 import bf16_value
+    return bf16_value(t.detach().cpu().view(torch.int16).numpy().view(np.uint16)).astype(np.float64)
+
+
+def _max_rel(got, ref):
+    return float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+
+
+def _fro_rel(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+@pytest.fixture(scope="module")
+def oracle_layers():
+    from _oracle_layers import OracleLayers
+    return OracleLayers(L)
+
+
+class Stack32:
+    def __init__(self):
+        lsn = _lsn()
+        from layer_streamed_nf4_quant_b300 import workload
+        self.desc = lsn.StackDesc(n_layers=L)
+        self.store = workload.build_store(self.desc)
+        self.resident = self.store.cuda()
+        self.lora = [workload.lora_blob(self.desc, l) for l in range(L)]
+        self.slots = [torch.empty(self.desc.image_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream()
+
+    def pool(self):
+        lsn = _lsn()
+        offs = [l * self.desc.image_bytes for l in range(L)]
+        return lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
+                              self.copy_stream)
+
+    def x0(self, M):
+        import synth
+        from layer_streamed_nf4_quant_b300 import workload
+        bits = synth.stack_input(M, self.desc.d_model)
+        return bits, workload.bf16_tensor(bits)
+
+    def run(self, M, pool=None, reference=False, layers_out=False, lora=None):
+        lsn = _lsn()
+        d = self.desc
+        _, x0 = self.x0(M)
+        grads = [torch.empty(d.lora_elems, dtype=torch.float32, device="cuda") for _ in range(L)]
+        loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+        x_out = torch.empty((M, d.d_model), dtype=torch.bfloat16, device="cuda")
+        dx0 = torch.empty((M, d.d_model), dtype=torch.float32, device="cuda")
+        x_ref = torch.empty((M, d.d_model), dtype=torch.bfloat16, device="cuda") if reference else None
+        xl = torch.empty((L, M, d.d_model), dtype=torch.bfloat16, device="cuda") if layers_out else None
+        dxl = torch.empty((L, M, d.d_model), dtype=torch.float32, device="cuda") if layers_out else None
+        ws = torch.empty(d.workspace_bytes(M, False, reference), dtype=torch.uint8, device="cuda")
+        lsn.layer_stack_step(d, x0, lora or self.lora, grads, loss, ws, pool=pool,
+                             resident_store=None if pool else self.resident, x_out=x_out, dx0=dx0,
+                             reference_pass=reference, x_ref_out=x_ref, x_layers_out=xl, dx_layers_out=dxl)
+        torch.cuda.synchronize()
+        assert lsn.device_check() == 0
+        del ws
+        return {"loss": loss, "x": x_out, "dx0": dx0, "grads": grads, "x_ref": x_ref, "xl": xl, "dxl": dxl}
+
+
+@pytest.fixture(scope="module")
+def stack32():
+    return Stack32()
+
+
+def _same(a, b):
+    assert torch.equal(a["loss"].view(torch.int32), b["loss"].view(torch.int32))
+    assert torch.equal(a["x"].view(torch.int16), b["x"].view(torch.int16))
+    assert torch.equal(a["dx0"].view(torch.int32), b["dx0"].view(torch.int32))
+    for g, h in zip(a["grads"], b["grads"]):
+        assert torch.equal(g.view(torch.int32), h.view(torch.int32))
+
+
+def _grads_np(desc, g):
+    A, B = desc.lora_views(g)
+    return ({p: v.double().cpu().numpy() for p, v in A.items()}, {p: v.double().cpu().numpy() for p, v in B.items()})
+
+
+def _rows(M, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 255, 256, 511, M // 2, M - 2, M - 1]
+    extra = rng.choice(M, 8, replace=False).tolist()
+    return np.array(sorted(set(r for r in fixed + extra if 0 <= r < M)))
+
+
+def test_stack32_512_oracle_parity_end_to_end_and_per_layer(stack32, oracle_layers):
+    from oracle import stack as ostack
+    M = 512
+    d = stack32.desc
+    pool = stack32.pool()
+    out = stack32.run(M, pool=pool, layers_out=True)
+    pool.close()
+    x0_bits, _ = stack32.x0(M)
+    from oracle.nf4 import bf16_value
+    x0 = bf16_value(x0_bits).astype(np.float64)
+
+    # end to end: the oracle's own 32-layer sweep
+    ref = ostack.stack_forward_backward(x0, oracle_layers, d.scale)
+    report = {"loss": abs(out["loss"].item() - ref["loss"]) / ref["loss"],
+              "x32": _max_rel(_f64_bits(out["x"]), ref["x_last"]),
+              "dx0": _fro_rel(out["dx0"].double().cpu().numpy(), ref["dx0"])}
+    worst = 0.0
+    for l in range(L):
+        gA, gB = _grads_np(d, out["grads"][l])
+        for p in gA:
+            worst = max(worst, _fro_rel(gA[p], ref["dA"][l][p]), _fro_rel(gB[p], ref["dB"][l][p]))
+    report["worst_grad"] = worst
+    xl_gpu = [_f64_bits(out["xl"][l]) for l in range(L)]
+    report["x_per_layer_e2e"] = [_max_rel(xl_gpu[l], ref["xs"][l + 1]) for l in range(L)]
+    del ref
+    print("stack32 512 end-to-end:", {k: v for k, v in report.items() if k != "x_per_layer_e2e"})
+    print("stack32 512 x_l vs oracle chain:", ["%.2e" % v for v in report["x_per_layer_e2e"]])
+    assert report["loss"] <= FWD_TOL and report["x32"] <= FWD_TOL, report
+    assert report["dx0"] <= GRAD_TOL and report["worst_grad"] <= GRAD_TOL, report
+
+    # teacher-forced: layer l of the oracle on the GPU's own x_l and dloss/dx_{l+1}
+    coef = 2.0 * 1e-3 / (M * d.d_kv)
+    tf = []
+    for l in range(L):
+        W, A, B = oracle_layers[l]
+        x_in = x0 if l == 0 else xl_gpu[l - 1]
+        x_next, cache = ostack.layer_forward(x_in, W, A, B, d.scale)
+        dx_next = xl_gpu[L - 1] / (M * d.d_model) if l == L - 1 else out["dxl"][l + 1].double().cpu().numpy()
+        dx, dA, dB = ostack.layer_backward(cache, dx_next, W, A, B, d.scale, coef * cache["k"], coef * cache["v"])
+        gA, gB = _grads_np(d, out["grads"][l])
+        e = {"x": _max_rel(xl_gpu[l], x_next), "dx": _fro_rel(out["dxl"][l].double().cpu().numpy(), dx),
+             "grad": max(max(_fro_rel(gA[p], dA[p]), _fro_rel(gB[p], dB[p])) for p in gA)}
+        tf.append(e)
+        assert e["x"] <= FWD_TOL and e["dx"] <= GRAD_TOL and e["grad"] <= GRAD_TOL, (l, e)
+    print("stack32 512 teacher-forced worst:", {k: max(e[k] for e in tf) for k in tf[0]})
+    # the gradient of the first layer's input is dx0
+    assert torch.equal(out["dxl"][0].view(torch.int32), out["dx0"].view(torch.int32))
+
+
+def test_stack32_16k_streamed_bit_identical_and_sampled_rows(stack32, oracle_layers):
+    from oracle import stack as ostack
+    from oracle.nf4 import bf16_value
+    M = 16384
+    d = stack32.desc
+    res = stack32.run(M)
+    pool = stack32.pool()
+    streamed = stack32.run(M, pool=pool)
+    st = pool.stats()
+    pool.close()
+    _same(res, streamed)
+    assert st["copies"] == 2 * L and np.isfinite(res["loss"].item())
+    del streamed
+    rows = _rows(M, seed=16)
+    x0_bits, _ = stack32.x0(M)
+    ref = ostack.stack_forward_backward(bf16_value(x0_bits[rows]).astype(np.float64), oracle_layers, d.scale,
+                                        token_count=M)
+    ix = torch.as_tensor(rows, device="cuda")
+    ex = _max_rel(_f64_bits(res["x"][ix]), ref["x_last"])
+    edx = _fro_rel(res["dx0"][ix].double().cpu().numpy(), ref["dx0"])
+    print(f"stack32 16k sampled rows ({len(rows)}): x32 {ex:.2e}  dx0 {edx:.2e}")
+    assert ex <= FWD_TOL and edx <= GRAD_TOL
+
+
+def test_stack32_preference_pair_reference_pass(stack32, oracle_layers):
+    from oracle import stack as ostack
+    from oracle.nf4 import bf16_value
+    M = 1024                       # chosen + rejected, 2 x 512 tokens
+    d = stack32.desc
+    pool = stack32.pool()
+    plain = stack32.run(M, pool=pool)
+    pool.reset_stats()
+    both = stack32.run(M, pool=pool, reference=True)
+    st = pool.stats()
+    pool.close()
+    _same(plain, both)                                        # the policy branch is unchanged
+    assert st["copies"] == 2 * L                              # bytes streamed per step x1.0
+    assert st["bytes_copied"] == 2 * L * d.image_bytes
+    rows = _rows(M, seed=4)
+    x0_bits, _ = stack32.x0(M)
+    x0r = bf16_value(x0_bits[rows]).astype(np.float64)
+    ix = torch.as_tensor(rows, device="cuda")
+    ref_frozen = ostack.frozen_stack_forward(x0r, (oracle_layers.weights(l) for l in range(L)))
+    e_ref = _max_rel(_f64_bits(both["x_ref"][ix]), ref_frozen)
+    ref_pol = ostack.stack_forward_backward(x0r, oracle_layers, d.scale, token_count=M)
+    e_pol = _max_rel(_f64_bits(both["x"][ix]), ref_pol["x_last"])
+    print(f"stack32 preference pair sampled rows ({len(rows)}): reference {e_ref:.2e}  policy {e_pol:.2e}")
+    assert e_ref <= FWD_TOL and e_pol <= FWD_TOL
+    assert np.max(np.abs(_f64_bits(both["x_ref"][ix]) - _f64_bits(both["x"][ix]))) > 0
+
+
+def test_stack32_zero_B_equals_reference_pass(stack32):
+    """B = 0 in all 32 layers: the policy forward is the frozen stack, bit for bit."""
+    d = stack32.desc
+    zeroed = []
+    for blob in stack32.lora:
+        z = blob.clone()
+        _, B = d.lora_views(z)
+        for p in B:
+            B[p].zero_()
+        zeroed.append(z)
+    out = stack32.run(512, reference=True, lora=zeroed)
+    assert torch.equal(out["x"].view(torch.int16), out["x_ref"].view(torch.int16))
