@@ -488,6 +488,9 @@ def main(argv=None):
                     help="read the layers from a resident device store instead of streaming them")
     ap.add_argument("--recompute", action="store_true",
                     help="keep only x_l per layer and recompute each layer in the reverse sweep")
+    ap.add_argument("--chunks", type=int, default=2, choices=[1, 2],
+                    help="copies per layer image: 2 = [header, q..up] and [o, down] (sub-layer streaming), "
+                         "1 = whole-layer copies")
     ap.add_argument("--show-ranks", action="store_true",
                     help="print each rank's world size, rank and device binding as JSON and exit")
     args = ap.parse_args(argv)
@@ -547,6 +550,8 @@ def main(argv=None):
     if not args.resident:
         pool = lsn.StreamPool(store, [l * desc.image_bytes for l in range(L)], desc.image_bytes, slots[0],
                               slots[1], copy)
+        if args.chunks == 2:
+            pool.set_chunks(desc.chunk_offsets())
     resident = store.to(dev) if args.resident else None
     setup_s = time.perf_counter() - t_setup
 
@@ -606,6 +611,7 @@ def main(argv=None):
                    "recompute": bool(args.recompute), "reference_pass": ref_pass,
                    "bytes_streamed_per_step_vs_plain_step":
                        (ps["bytes_copied"] / args.steps) / (2 * L * desc.image_bytes) if ps else 0.0,
+                   "copies_per_layer_image": args.chunks if resident is None else 0,
                    "streamed_bytes_per_step": streamed_bytes, "l2": "inputs larger than L2 "
                    f"({streamed_bytes / 1e9:.2f} GB of layer images streamed per step)",
                    "parallelism": f"replicas x{world}"},

@@ -211,6 +211,32 @@ int stream_pool_release(lsn_pool* pool, int layer, void* compute_stream);
 /* Synchronises the copy stream and fills *out. */
 int stream_pool_stats(lsn_pool* pool, lsn_pool_stats* out);
 int stream_pool_reset_stats(lsn_pool* pool);
+/* Sub-layer streaming.  Splits every layer image into n_chunks byte ranges [chunk_offset[c],
+ * chunk_offset[c + 1]) with chunk_offset[0] = 0, ascending, 256-byte aligned, the last chunk
+ * ending at layer_bytes (chunk_offset: host array of n_chunks, 1 <= n_chunks <= 8; ignored for
+ * n_chunks = 1).  A prefetch then issues one cudaMemcpyAsync per chunk, each followed by that
+ * chunk's copy-done event, so the compute stream can start on the chunks it needs first
+ * (stream_pool_wait_range) while the others are still copying.  Bytes and results are the
+ * same as with whole-layer copies.  LSN_ESTATE while a slot holds a prefetched or waited
+ * layer (call it before the first prefetch or after every layer is released); it forgets the
+ * slots' contents.  [P1] "Did a correctness bug invalidate the Llama 3.1 8B result?": the
+ * pages' wrong-gradient bug lived in how large layers were transferred; the tests check the
+ * chunked stream bit for bit against the resident run on a layer above 172 MiB. */
+int stream_pool_set_chunks(lsn_pool* pool, int n_chunks, const size_t* chunk_offset);
+/* stream_pool_prefetch with the chunk order: ascending (reverse == 0) or descending.  The
+ * reverse sweep of layer_stack_step copies o and down (the end of the image) first because
+ * its backward needs them first.  stream_pool_prefetch(pool, l) is
+ * stream_pool_prefetch_ex(pool, l, 0). */
+int stream_pool_prefetch_ex(lsn_pool* pool, int layer, int reverse);
+/* stream_pool_wait for the bytes [begin, end) of the layer image only: the compute stream
+ * waits for the copy-done event of the last chunk, in this prefetch's copy order, that covers
+ * the range (chunks land in copy order on the one copy stream).  LSN_EINVAL if the range is
+ * empty or outside the image.  stream_pool_wait is the range [0, layer_bytes). */
+int stream_pool_wait_range(lsn_pool* pool, int layer, size_t begin, size_t end, void* compute_stream,
+                           const void** dev_image, int timeout_ms);
+/* Statistics of one chunk index over all layers (synchronises the copy stream): bytes_copied,
+ * copies and copy_ms of that chunk's transfers; the other fields are zero. */
+int stream_pool_chunk_stats(lsn_pool* pool, int chunk, lsn_pool_stats* out);
 /* Fault injection for tests: every later prefetch first runs a host callback on the copy
  * stream that sleeps `usec` microseconds (0 turns it off, at most 10 s).  Results must not
  * change; only the copies come later. */

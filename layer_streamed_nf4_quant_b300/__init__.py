@@ -186,13 +186,29 @@ class StreamPool:
                                      first_slot, 1 if reuse_resident else 0, C.byref(h)))
         self.handle = h
 
-    def prefetch(self, layer: int):
-        check(lib.stream_pool_prefetch(self.handle, layer))
+    def prefetch(self, layer: int, reverse: bool = False):
+        check(lib.stream_pool_prefetch_ex(self.handle, layer, 1 if reverse else 0))
 
     def wait(self, layer: int, stream=None, timeout_ms: int = 0) -> int:
         p = C.c_void_p()
         check(lib.stream_pool_wait(self.handle, layer, _stream(stream), C.byref(p), timeout_ms))
         return p.value
+
+    def wait_range(self, layer: int, begin: int, end: int, stream=None, timeout_ms: int = 0) -> int:
+        p = C.c_void_p()
+        check(lib.stream_pool_wait_range(self.handle, layer, begin, end, _stream(stream), C.byref(p), timeout_ms))
+        return p.value
+
+    def set_chunks(self, offsets):
+        """Copy every layer as len(offsets) chunks starting at these byte offsets (offsets[0] = 0)."""
+        n = len(offsets)
+        arr = (C.c_size_t * n)(*[int(o) for o in offsets])
+        check(lib.stream_pool_set_chunks(self.handle, n, arr))
+
+    def chunk_stats(self, chunk: int) -> dict:
+        s = lsn_pool_stats()
+        check(lib.stream_pool_chunk_stats(self.handle, chunk, C.byref(s)))
+        return {"bytes_copied": s.bytes_copied, "copies": s.copies, "copy_ms": s.copy_ms}
 
     def release(self, layer: int, stream=None):
         check(lib.stream_pool_release(self.handle, layer, _stream(stream)))
@@ -241,6 +257,11 @@ class StackDesc:
         lo = (C.c_size_t * 14)()
         check(lib.lsn_lora_offsets(C.byref(self.c), lo))
         self.lora_offsets = list(lo)
+
+    def chunk_offsets(self):
+        """Byte offsets of the two sub-layer chunks of an image: [header, q, k, v, gate, up]
+        and [o, down] (the parts the forward needs first and the backward needs first)."""
+        return [0, self.image_offsets[PROJ.index("o")]]
 
     def shape(self, p: str):
         D, dkv, F = self.d_model, self.d_kv, self.d_ff

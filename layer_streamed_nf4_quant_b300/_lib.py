@@ -90,6 +90,10 @@ SIGNATURES = {
     "stream_pool_stats": (I, [P, C.POINTER(lsn_pool_stats)]),
     "stream_pool_reset_stats": (I, [P]),
     "stream_pool_set_copy_delay_us": (I, [P, I]),
+    "stream_pool_set_chunks": (I, [P, I, C.POINTER(SZ)]),
+    "stream_pool_prefetch_ex": (I, [P, I, I]),
+    "stream_pool_wait_range": (I, [P, I, SZ, SZ, P, C.POINTER(P), I]),
+    "stream_pool_chunk_stats": (I, [P, I, C.POINTER(lsn_pool_stats)]),
     "stream_pool_destroy": (I, [P]),
     "lsn_layer_image_bytes": (SZ, [C.POINTER(lsn_stack_desc)]),
     "lsn_layer_image_offsets": (I, [C.POINTER(lsn_stack_desc), C.POINTER(SZ)]),

@@ -162,7 +162,21 @@ struct Ctx {
     bool dry = false;
     size_t partial_need = 0;
     size_t img_off[kNumProj];
+    size_t img_bytes = 0;
     size_t la[kNumProj], lb[kNumProj];   // LoRA element offsets (A_p, B_p)
+    // streamed mode: the layer being computed; need() makes the compute stream wait for a byte
+    // range of its image (a no-op for a resident store, or when nothing is being computed)
+    lsn_pool* pool = nullptr;
+    int layer = -1;
+
+    int need(size_t begin, size_t end) {
+        if (dry || !pool || layer < 0) return LSN_OK;
+        const void* p = nullptr;
+        return stream_pool_wait_range(pool, layer, begin, end, s, &p, 0);
+    }
+    // the header and q, k, v, gate, up / o and down
+    int need_qkvgu() { return need(0, img_off[kO]); }
+    int need_od() { return need(img_off[kO], img_bytes); }
 
     int run(GemmPlan& g) {
         if (g.status()) return g.status();
@@ -235,6 +249,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         RC(c.run(g));
     }
     if (recompute) return LSN_OK;
+    RC(c.need_od());
     {   // x' = bf16(x + q W_o^T + a W_d^T + s T_o B_o^T + s T_d B_d^T)
         GemmPlan g(c.dry);
         int mq = g.map(b.y[l], M, D, d.Ncat, kBM);
@@ -300,7 +315,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
     const Dims& d = c.d;
     const Buffers& b = c.b;
     const int M = d.M, D = d.D, F = d.F, r = d.r;
-    if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
+    RC(c.need_od());
     {   // dT_o = bf16(s dx' B_o), dT_d = bf16(s dx' B_d)
         GemmPlan g(c.dry);
         int mdx = g.map(b.dx_bf, M, D, D, kBM);
@@ -347,6 +362,8 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
     }
     if (!c.dry)
         RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / ((double)M * d.dkv)), c.s));
+    RC(c.need_qkvgu());
+    if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
     {   // dT_p = bf16(s dY_p B_p)
         GemmPlan g(c.dry);
         int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
@@ -397,6 +414,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
 int init_ctx(Ctx& c, const lsn_stack_desc* desc, int64_t M) {
     if (!make_dims(desc, M, &c.d)) return fail(LSN_EINVAL, "layer stack: bad descriptor or M");
     RC(lsn_layer_image_offsets(desc, c.img_off));
+    c.img_bytes = lsn_layer_image_bytes(desc);
     size_t lo[2 * kNumProj];
     RC(lsn_lora_offsets(desc, lo));
     for (int p = 0; p < kNumProj; ++p) {
@@ -466,28 +484,33 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
     if (ws_bytes < need) return fail(LSN_ENOMEM, "layer_stack_step: workspace %zu < %zu", ws_bytes, need);
     layout(c.d, static_cast<uint8_t*>(ws), x0, &c.b, pneed, c.o);
     c.s = static_cast<cudaStream_t>(stream);
-    const size_t img_bytes = lsn_layer_image_bytes(desc);
+    const size_t img_bytes = c.img_bytes;
     const uint8_t* res = static_cast<const uint8_t*>(resident_store);
     const int L = c.d.L;
-    auto image = [&](int l, const uint8_t** img) -> int {
+    c.pool = pool;
+    // the layer's image address; streamed, the compute stream first waits for the part of it
+    // the layer's first GEMMs read (the rest is waited for by Ctx::need before its GEMMs)
+    auto image = [&](int l, bool od_first, const uint8_t** img) -> int {
+        c.layer = l;
         if (!pool) {
             *img = res + (size_t)l * img_bytes;
             return LSN_OK;
         }
         const void* p = nullptr;
-        int rc = stream_pool_wait(pool, l, stream, &p, 0);
+        int rc = od_first ? stream_pool_wait_range(pool, l, c.img_off[kO], img_bytes, stream, &p, 0)
+                          : stream_pool_wait_range(pool, l, 0, c.img_off[kO], stream, &p, 0);
         *img = static_cast<const uint8_t*>(p);
         return rc;
     };
 
     // forward sweep, prefetching one layer ahead; the reference pass (if any) runs on the
     // same slot before it is released, so it costs no extra copy
-    if (pool) RC(stream_pool_prefetch(pool, 0));
+    if (pool) RC(stream_pool_prefetch_ex(pool, 0, 0));
     const uint16_t* xr_in = x0;
     for (int l = 0; l < L; ++l) {
-        if (pool && l + 1 < L) RC(stream_pool_prefetch(pool, l + 1));
+        if (pool && l + 1 < L) RC(stream_pool_prefetch_ex(pool, l + 1, 0));
         const uint8_t* img;
-        RC(image(l, &img));
+        RC(image(l, false, &img));
         RC(fwd_layer(c, l, img, lora[l]));
         if (c.o.reference_pass) {
             uint16_t* xr_out = c.b.xr[l & 1];
@@ -503,12 +526,16 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
                                          cudaMemcpyDeviceToDevice, c.s));
     RC(launch_loss(c.b.x[L], c.d.M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart, loss_out,
                    c.s));
-    // reverse sweep, re-streaming every layer (and recomputing its activations if asked)
-    if (pool) RC(stream_pool_prefetch(pool, L - 1));
+    // reverse sweep, re-streaming every layer (and recomputing its activations if asked); the
+    // backward of a layer starts with o and down, so those are copied first -- unless the
+    // layer is recomputed, which starts with q..up
+    c.layer = -1;
+    const int rev = c.o.recompute ? 0 : 1;
+    if (pool) RC(stream_pool_prefetch_ex(pool, L - 1, rev));
     for (int l = L - 1; l >= 0; --l) {
-        if (pool && l - 1 >= 0) RC(stream_pool_prefetch(pool, l - 1));
+        if (pool && l - 1 >= 0) RC(stream_pool_prefetch_ex(pool, l - 1, rev));
         const uint8_t* img;
-        RC(image(l, &img));
+        RC(image(l, rev != 0, &img));
         if (c.o.recompute) RC(fwd_layer(c, l, img, lora[l], true));
         RC(bwd_layer(c, l, img, lora[l], grads[l]));
         if (c.o.dx_layers_out)
@@ -521,6 +548,7 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         }
         if (pool) RC(stream_pool_release(pool, l, stream));
     }
+    c.layer = -1;
     if (x_out)
         LSN_CUDA_TRY(cudaMemcpyAsync(x_out, c.b.x[L], (size_t)c.d.M * c.d.D * 2, cudaMemcpyDeviceToDevice, c.s));
     if (x_ref_out && c.o.reference_pass)

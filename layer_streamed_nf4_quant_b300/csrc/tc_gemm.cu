@@ -506,33 +506,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             uint32_t n_steps = 0;
             for (uint32_t i = 0; s.t < p.total_tiles; ++i, seq_next(p, s, rank)) {
                 const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
-                if (!ptx::mbar_wait_bounded_cta(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyTma))
-                    break;
+                // everything the copies need is read before the stage is free
                 const Problem& pr = p.probs[s.ti.prob];
                 const KSeg& sg = p.segs[s.si];
                 const int half = pr.bn >> 1;
                 const uint32_t bar = full_bar(stage);
                 const uint32_t a_dst = sA + stage * kStageABytes;
                 const uint32_t b_dst = sB + stage * kStageBBytes;
-                uint32_t bytes = kStageABytes;
-                if (sg.b_src == B_TMA_K || sg.b_src == B_TMA_MN) bytes += half * kBK * 2;
-                ptx::mbar_arrive_expect_tx(bar, bytes);
+                const int bsrc = sg.b_src;
+                const uint32_t bytes = kStageABytes + ((bsrc == B_TMA_K || bsrc == B_TMA_MN) ? half * kBK * 2 : 0);
                 const int ak = sg.a_k0 + s.kk * kBK;
-                if (pr.a_major == A_KMAJOR) {
-                    ptx::tma_load_2d_hint(a_dst, &p.maps[sg.a_map], ak, s.ti.m0, bar, pol_keep);
+                const bool a_k = pr.a_major == A_KMAJOR;
+                const CUtensorMap* amap = &p.maps[sg.a_map];
+                const CUtensorMap* bmap = &p.maps[sg.b_idx];
+                const int bk = sg.b_k0 + s.kk * kBK;
+                const int nb = sg.b_n0 + s.ti.n0 + (int)rank * half;
+                const int m0 = s.ti.m0;
+                if (!ptx::mbar_wait_bounded_cta(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyTma))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar, bytes);
+                if (a_k) {
+                    ptx::tma_load_2d_hint(a_dst, amap, ak, m0, bar, pol_keep);
                 } else {
 #pragma unroll
                     for (int q = 0; q < kBM / 64; ++q)
-                        ptx::tma_load_2d_hint(a_dst + q * 8192, &p.maps[sg.a_map], s.ti.m0 + 64 * q, ak, bar,
-                                              pol_keep);
+                        ptx::tma_load_2d_hint(a_dst + q * 8192, amap, m0 + 64 * q, ak, bar, pol_keep);
                 }
-                const int bk = sg.b_k0 + s.kk * kBK;
-                const int nb = sg.b_n0 + s.ti.n0 + (int)rank * half;
-                if (sg.b_src == B_TMA_K) {
-                    ptx::tma_load_2d(b_dst, &p.maps[sg.b_idx], bk, nb, bar);
-                } else if (sg.b_src == B_TMA_MN) {
+                if (bsrc == B_TMA_K) {
+                    ptx::tma_load_2d(b_dst, bmap, bk, nb, bar);
+                } else if (bsrc == B_TMA_MN) {
                     for (int q = 0; q < half / 64; ++q)
-                        ptx::tma_load_2d(b_dst + q * 8192, &p.maps[sg.b_idx], nb + 64 * q, bk, bar);
+                        ptx::tma_load_2d(b_dst + q * 8192, bmap, nb + 64 * q, bk, bar);
                 }
                 n_steps = i + 1;
             }
@@ -711,6 +715,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 if (nxt.kind == kJobNf4) nf4_load_block(p.nf4[nxt.w], nxt.row, nxt.col0, nb);
             }
             const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+            // the row is decoded into registers before the stage is free; only the stores wait
+            uint32_t o[32];
+            if (cur.kind == kJobNf4) {
+                nf4_decode_regs(cb, p.levels, o);
+            } else if (cur.kind == kJobScaled) {
+                scaled_row(cur.sp, cur.sk, cur.ss, o);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = 0u;
+            }
             int ok = 0;
             if (lane == 0)
                 ok = ptx::mbar_wait_bounded_cta(empty_bar(stage), phase ^ 1u, abort_flag, p.err, kSiteEmptyDeq);
@@ -718,15 +732,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             if (!ok) break;
             if (cur.kind != kJobNone) {
                 const uint32_t dst = sB + stage * kStageBBytes + cur.dst_off;
-                uint32_t o[32];
-                if (cur.kind == kJobNf4) {
-                    nf4_decode_regs(cb, p.levels, o);
-                } else if (cur.kind == kJobScaled) {
-                    scaled_row(cur.sp, cur.sk, cur.ss, o);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = 0u;
-                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
                     st_shared_v4(dst + (uint32_t)((ch ^ (int)cur.swz) << 4), o[4 * ch], o[4 * ch + 1],

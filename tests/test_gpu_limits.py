@@ -34,6 +34,10 @@ def test_layer_image_above_172_mib_streamed_equals_resident():
     for g in res["grads"]:
         assert torch.isfinite(g).all() and (g != 0).any()
     pool.close()
+    pool = st.pool(chunked=True)                              # sub-layer chunks of such a layer
+    _same(res, st.run(pool))
+    assert pool.chunk_stats(1)["copies"] == 2 * desc.n_layers
+    pool.close()
 
 
 def test_weight_above_2pow31_nibbles_sampled_parity():

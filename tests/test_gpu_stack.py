@@ -36,11 +36,14 @@ class Stack:
         self.slots = [torch.empty(desc.image_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
         self.copy_stream = torch.cuda.Stream()
 
-    def pool(self, first_slot=0, reuse=False):
+    def pool(self, first_slot=0, reuse=False, chunked=False):
         lsn = _lsn()
         offs = [l * self.desc.image_bytes for l in range(self.desc.n_layers)]
-        return lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
+        pool = lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
                               self.copy_stream, first_slot=first_slot, reuse_resident=reuse)
+        if chunked:
+            pool.set_chunks(self.desc.chunk_offsets())
+        return pool
 
     def run(self, pool=None, recompute=False, reference=False):
         lsn = _lsn()
@@ -222,6 +225,60 @@ def test_host_wait_timeout_then_recovery(small):
     pool.release(0)
     pool.set_copy_delay_us(0)
     _same(base, small.run(pool))
+    pool.close()
+
+
+def test_chunked_stream_bit_identical_to_resident(small):
+    """Sub-layer streaming: each layer copied as [header, q..up] and [o, down], ascending in
+    the forward sweep and descending in the reverse one, each GEMM group waiting only for its
+    own chunk.  Same bits as the resident run, plain, recomputed and with the reference pass;
+    every chunk of every layer copied once per sweep."""
+    d = small.desc
+    base = small.run()
+    pool = small.pool(chunked=True)
+    _same(base, small.run(pool))
+    st = pool.stats()
+    assert st["copies"] == 2 * d.n_layers and st["bytes_copied"] == 2 * d.n_layers * d.image_bytes
+    c0, c1 = pool.chunk_stats(0), pool.chunk_stats(1)
+    assert c0["copies"] == c1["copies"] == 2 * d.n_layers
+    assert c0["bytes_copied"] == 2 * d.n_layers * d.chunk_offsets()[1]
+    assert c0["bytes_copied"] + c1["bytes_copied"] == st["bytes_copied"]
+    _same(base, small.run(pool, recompute=True))
+    _same(base, small.run(pool, reference=True))
+    pool.set_copy_delay_us(2000)                              # late chunks change nothing
+    _same(base, small.run(pool))
+    pool.close()
+    pool = small.pool(first_slot=1, reuse=True, chunked=True)
+    _same(base, small.run(pool))
+    pool.close()
+
+
+def test_chunk_validation_and_range_waits(small):
+    lsn = _lsn()
+    d = small.desc
+    pool = small.pool()
+    o = d.chunk_offsets()[1]
+    for bad in ([0, o + 1], [0, 0], [0, d.image_bytes], [256, o], [0, o, o]):
+        with pytest.raises(lsn.LsnError) as e:
+            pool.set_chunks(bad)
+        assert e.value.code == lsn.LSN_EINVAL
+    pool.set_chunks([0, o])
+    pool.prefetch(0, reverse=True)
+    with pytest.raises(lsn.LsnError) as e:
+        pool.set_chunks([0])                                  # a slot holds layer 0
+    assert e.value.code == lsn.LSN_ESTATE
+    with pytest.raises(lsn.LsnError) as e:
+        pool.wait_range(0, o, o)                              # empty range
+    assert e.value.code == lsn.LSN_EINVAL
+    a = pool.wait_range(0, o, d.image_bytes)                  # the chunk copied first
+    b = pool.wait_range(0, 0, 64)                             # the header, copied second
+    assert a == b
+    torch.cuda.synchronize()
+    img = torch.empty(d.image_bytes, dtype=torch.uint8, device="cuda")
+    img.copy_(small.slots[0])
+    assert torch.equal(img.cpu(), small.store[:d.image_bytes])
+    pool.release(0)
+    pool.set_chunks([0])                                      # back to whole-layer copies
     pool.close()
 
 
