@@ -14,9 +14,17 @@ oracle (the oracle quantises and dequantises all 32 layers itself; see _oracle_l
   slots against the oracle's frozen stack on sampled rows, with no extra layer copies.
 * B = 0 in every layer: the policy stack equals the reference pass bit for bit.
 
-Bars: forward max|y - y_ref| / max|y_ref| <= 2e-2; gradients ||g - g_ref||_F / ||g_ref||_F
-<= 1e-2; streamed against resident bit-identical.
+Bars.  One layer on its own inputs (teacher-forced): forward max|y - y_ref| / max|y_ref|
+<= 2e-2, gradients ||g - g_ref||_F / ||g_ref||_F <= 1e-2.  End to end over 32 layers the
+bf16 roundings of every layer compound: a twin of the oracle with the same rounding points
+and fp32-accumulated products (what tensor cores do) already drifts from the fp64 oracle by
+about 2.6e-2 (x_32), 3.1e-2 (dx0) and 3.8e-2 (dA, dB), measured by golden/stack_drift.py
+into golden/stack_drift.json.  The end-to-end bars are 1.5 times that drift, and never
+tighter than the one-layer bars.  Streamed against resident: bit-identical.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -26,6 +34,15 @@ pytestmark = pytest.mark.gpu
 FWD_TOL = 2e-2
 GRAD_TOL = 1e-2
 L = 32
+
+
+def _e2e_bars():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "stack_drift.json")) as f:
+        rec = json.load(f)
+    d = rec["fp32_twin_vs_oracle"]
+    return {"x": max(FWD_TOL, 1.5 * d["x_L_max_rel"]), "dx0": max(GRAD_TOL, 1.5 * d["dx0_fro_rel"]),
+            "grad": max(GRAD_TOL, 1.5 * d["worst_grad_fro_rel"]),
+            "frozen": max(FWD_TOL, 1.5 * rec["fp32_twin_frozen_vs_oracle_frozen"]["x_L_max_rel"])}
 
 
 def _lsn():
@@ -63,11 +80,14 @@ class Stack32:
         self.slots = [torch.empty(self.desc.image_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
         self.copy_stream = torch.cuda.Stream()
 
-    def pool(self):
+    def pool(self, chunked=False):
         lsn = _lsn()
         offs = [l * self.desc.image_bytes for l in range(L)]
-        return lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
+        pool = lsn.StreamPool(self.store, offs, self.desc.image_bytes, self.slots[0], self.slots[1],
                               self.copy_stream)
+        if chunked:
+            pool.set_chunks(self.desc.chunk_offsets())
+        return pool
 
     def x0(self, M):
         import synth
@@ -121,19 +141,52 @@ def _rows(M, seed):
     return np.array(sorted(set(r for r in fixed + extra if 0 <= r < M)))
 
 
-def test_stack32_512_oracle_parity_end_to_end_and_per_layer(stack32, oracle_layers):
-    from oracle import stack as ostack
-    M = 512
-    d = stack32.desc
+@pytest.fixture(scope="module")
+def run512(stack32):
+    """The streamed 32-layer step at batch 1 x 512 tokens with every layer's x and dx kept."""
     pool = stack32.pool()
-    out = stack32.run(M, pool=pool, layers_out=True)
+    out = stack32.run(512, pool=pool, layers_out=True)
     pool.close()
-    x0_bits, _ = stack32.x0(M)
+    x0_bits, _ = stack32.x0(512)
     from oracle.nf4 import bf16_value
-    x0 = bf16_value(x0_bits).astype(np.float64)
+    out["x0"] = bf16_value(x0_bits).astype(np.float64)
+    out["xl_np"] = [_f64_bits(out["xl"][l]) for l in range(L)]
+    return out
 
-    # end to end: the oracle's own 32-layer sweep
-    ref = ostack.stack_forward_backward(x0, oracle_layers, d.scale)
+
+def test_stack32_512_teacher_forced_every_layer(stack32, oracle_layers, run512):
+    """Layer l of the oracle on the GPU's own x_l (forward) and dloss/dx_{l+1} (backward):
+    each layer of the GPU stack within the bars on its own inputs."""
+    from oracle import stack as ostack
+    M, d, out = 512, stack32.desc, run512
+    coef = 2.0 * 1e-3 / (M * d.d_kv)
+    tf = []
+    for l in range(L):
+        W, A, B = oracle_layers[l]
+        x_in = out["x0"] if l == 0 else out["xl_np"][l - 1]
+        x_next, cache = ostack.layer_forward(x_in, W, A, B, d.scale)
+        if l == L - 1:
+            dx_next = out["xl_np"][L - 1] / (M * d.d_model)
+        else:
+            dx_next = out["dxl"][l + 1].double().cpu().numpy()
+        dx, dA, dB = ostack.layer_backward(cache, dx_next, W, A, B, d.scale, coef * cache["k"], coef * cache["v"])
+        gA, gB = _grads_np(d, out["grads"][l])
+        e = {"x": _max_rel(out["xl_np"][l], x_next), "dx": _fro_rel(out["dxl"][l].double().cpu().numpy(), dx),
+             "grad": max(max(_fro_rel(gA[p], dA[p]), _fro_rel(gB[p], dB[p])) for p in gA)}
+        tf.append(e)
+    print("stack32 512 teacher-forced per layer:",
+          [("%.1e %.1e %.1e" % (e["x"], e["dx"], e["grad"])) for e in tf])
+    for l, e in enumerate(tf):
+        assert e["x"] <= FWD_TOL and e["dx"] <= GRAD_TOL and e["grad"] <= GRAD_TOL, (l, e)
+    # the gradient of the first layer's input is dx0
+    assert torch.equal(out["dxl"][0].view(torch.int32), out["dx0"].view(torch.int32))
+
+
+def test_stack32_512_oracle_parity_end_to_end(stack32, oracle_layers, run512):
+    """The oracle's own 32-layer sweep against the GPU's: loss, x_32, dx0, every dA_p, dB_p."""
+    from oracle import stack as ostack
+    d, out = stack32.desc, run512
+    ref = ostack.stack_forward_backward(out["x0"], oracle_layers, d.scale)
     report = {"loss": abs(out["loss"].item() - ref["loss"]) / ref["loss"],
               "x32": _max_rel(_f64_bits(out["x"]), ref["x_last"]),
               "dx0": _fro_rel(out["dx0"].double().cpu().numpy(), ref["dx0"])}
@@ -143,31 +196,12 @@ def test_stack32_512_oracle_parity_end_to_end_and_per_layer(stack32, oracle_laye
         for p in gA:
             worst = max(worst, _fro_rel(gA[p], ref["dA"][l][p]), _fro_rel(gB[p], ref["dB"][l][p]))
     report["worst_grad"] = worst
-    xl_gpu = [_f64_bits(out["xl"][l]) for l in range(L)]
-    report["x_per_layer_e2e"] = [_max_rel(xl_gpu[l], ref["xs"][l + 1]) for l in range(L)]
-    del ref
-    print("stack32 512 end-to-end:", {k: v for k, v in report.items() if k != "x_per_layer_e2e"})
-    print("stack32 512 x_l vs oracle chain:", ["%.2e" % v for v in report["x_per_layer_e2e"]])
-    assert report["loss"] <= FWD_TOL and report["x32"] <= FWD_TOL, report
-    assert report["dx0"] <= GRAD_TOL and report["worst_grad"] <= GRAD_TOL, report
-
-    # teacher-forced: layer l of the oracle on the GPU's own x_l and dloss/dx_{l+1}
-    coef = 2.0 * 1e-3 / (M * d.d_kv)
-    tf = []
-    for l in range(L):
-        W, A, B = oracle_layers[l]
-        x_in = x0 if l == 0 else xl_gpu[l - 1]
-        x_next, cache = ostack.layer_forward(x_in, W, A, B, d.scale)
-        dx_next = xl_gpu[L - 1] / (M * d.d_model) if l == L - 1 else out["dxl"][l + 1].double().cpu().numpy()
-        dx, dA, dB = ostack.layer_backward(cache, dx_next, W, A, B, d.scale, coef * cache["k"], coef * cache["v"])
-        gA, gB = _grads_np(d, out["grads"][l])
-        e = {"x": _max_rel(xl_gpu[l], x_next), "dx": _fro_rel(out["dxl"][l].double().cpu().numpy(), dx),
-             "grad": max(max(_fro_rel(gA[p], dA[p]), _fro_rel(gB[p], dB[p])) for p in gA)}
-        tf.append(e)
-        assert e["x"] <= FWD_TOL and e["dx"] <= GRAD_TOL and e["grad"] <= GRAD_TOL, (l, e)
-    print("stack32 512 teacher-forced worst:", {k: max(e[k] for e in tf) for k in tf[0]})
-    # the gradient of the first layer's input is dx0
-    assert torch.equal(out["dxl"][0].view(torch.int32), out["dx0"].view(torch.int32))
+    per_layer = [_max_rel(out["xl_np"][l], ref["xs"][l + 1]) for l in range(L)]
+    bars = _e2e_bars()
+    print("stack32 512 end-to-end:", report, "bars:", bars)
+    print("stack32 512 x_l vs oracle chain:", ["%.2e" % v for v in per_layer])
+    assert report["loss"] <= FWD_TOL and report["x32"] <= bars["x"], report
+    assert report["dx0"] <= bars["dx0"] and report["worst_grad"] <= bars["grad"], report
 
 
 def test_stack32_16k_streamed_bit_identical_and_sampled_rows(stack32, oracle_layers):
@@ -190,8 +224,9 @@ def test_stack32_16k_streamed_bit_identical_and_sampled_rows(stack32, oracle_lay
     ix = torch.as_tensor(rows, device="cuda")
     ex = _max_rel(_f64_bits(res["x"][ix]), ref["x_last"])
     edx = _fro_rel(res["dx0"][ix].double().cpu().numpy(), ref["dx0"])
-    print(f"stack32 16k sampled rows ({len(rows)}): x32 {ex:.2e}  dx0 {edx:.2e}")
-    assert ex <= FWD_TOL and edx <= GRAD_TOL
+    bars = _e2e_bars()
+    print(f"stack32 16k sampled rows ({len(rows)}): x32 {ex:.2e}  dx0 {edx:.2e}  bars {bars}")
+    assert ex <= bars["x"] and edx <= bars["dx0"]
 
 
 def test_stack32_preference_pair_reference_pass(stack32, oracle_layers):
@@ -216,9 +251,19 @@ def test_stack32_preference_pair_reference_pass(stack32, oracle_layers):
     e_ref = _max_rel(_f64_bits(both["x_ref"][ix]), ref_frozen)
     ref_pol = ostack.stack_forward_backward(x0r, oracle_layers, d.scale, token_count=M)
     e_pol = _max_rel(_f64_bits(both["x"][ix]), ref_pol["x_last"])
+    bars = _e2e_bars()
     print(f"stack32 preference pair sampled rows ({len(rows)}): reference {e_ref:.2e}  policy {e_pol:.2e}")
-    assert e_ref <= FWD_TOL and e_pol <= FWD_TOL
+    assert e_ref <= bars["frozen"] and e_pol <= bars["x"]
     assert np.max(np.abs(_f64_bits(both["x_ref"][ix]) - _f64_bits(both["x"][ix]))) > 0
+
+
+def test_stack32_512_chunked_stream_bit_identical(stack32, run512):
+    """The headline configuration streamed in sub-layer chunks gives the whole-layer streamed
+    run's bits (which the tests above check against the oracle)."""
+    pool = stack32.pool(chunked=True)
+    out = stack32.run(512, pool=pool)
+    pool.close()
+    _same(run512, out)
 
 
 def test_stack32_zero_B_equals_reference_pass(stack32):
