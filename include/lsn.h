@@ -141,6 +141,15 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M,
                  const uint16_t* residual /* nullable */, uint16_t* Y, uint16_t* T_out,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* Diagnostics (host only, no device work): the split-K counts lora_nf4_fwd uses for this shape
+ * in its two launches -- T = X A^T and Y = X W^T + s T B^T -- and the fp32 partial-sum bytes
+ * each launch needs (0 when it is not split).  The counts come from the library's launch
+ * planner, which replays the GEMM's static tile schedule on a fixed 148-SM machine, so they
+ * (and the summation order they fix) do not depend on the device.  Every output pointer is
+ * nullable.  LSN_EINVAL for a shape lora_nf4_fwd refuses. */
+int lora_nf4_fwd_plan(int64_t M, int64_t n_out, int64_t k_in, int r, int* t_splits, int* y_splits,
+                      size_t* t_partial_bytes, size_t* y_partial_bytes);
+
 /* lora_nf4_fwd for callers that cannot allocate device memory (a plug-in inside a framework
  * that owns all device memory, or a serving path that must not enter the allocator).  The
  * pages have no counterpart of it.  Same arguments and results as lora_nf4_fwd, bit for bit,

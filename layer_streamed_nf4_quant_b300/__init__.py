@@ -99,6 +99,13 @@ def lora_nf4_fwd(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, 
     return Y, T
 
 
+def lora_fwd_plan(M: int, n_out: int, k_in: int, r: int) -> dict:
+    """Split-K counts and partial-sum bytes of lora_nf4_fwd's two launches for this shape."""
+    ts, ys, tb, yb = C.c_int(), C.c_int(), C.c_size_t(), C.c_size_t()
+    check(lib.lora_nf4_fwd_plan(M, n_out, k_in, r, C.byref(ts), C.byref(ys), C.byref(tb), C.byref(yb)))
+    return {"t_splits": ts.value, "y_splits": ys.value, "t_partial_bytes": tb.value, "y_partial_bytes": yb.value}
+
+
 def lora_nf4_fwd_static_scratch(packed, n_out, k_in, X, A, B, r, scale, residual=None, Y=None, T=None,
                                 sync_status=False, stream=None):
     """lora_nf4_fwd without a workspace or any device allocation, for callers that may not

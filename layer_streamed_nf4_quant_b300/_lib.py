@@ -81,6 +81,7 @@ SIGNATURES = {
     "lora_nf4_workspace_bytes": (SZ, [I64, I64, I64, I]),
     "lora_nf4_fwd": (I, [C.POINTER(nf4_view), P, I64, P, P, I, F, P, P, P, P, SZ, P]),
     "lora_nf4_bwd": (I, [C.POINTER(nf4_view), P, P, P, I64, P, P, I, F, P, I, P, P, P, SZ, P]),
+    "lora_nf4_fwd_plan": (I, [I64, I64, I64, I, C.POINTER(I), C.POINTER(I), C.POINTER(SZ), C.POINTER(SZ)]),
     "lora_nf4_fwd_static_scratch": (I, [C.POINTER(nf4_view), P, I64, P, P, I, F, P, P, P, C.POINTER(C.c_uint32),
                                         P]),
     "stream_pool_create": (I, [P, SZ, C.POINTER(SZ), SZ, I, P, P, P, I, I, C.POINTER(P)]),

@@ -235,7 +235,7 @@ __global__ void dy_build_kernel(const float* __restrict__ dqa, const uint16_t* _
                                 uint16_t* __restrict__ dy, int M, int D, int dkv, int F, float kv_coef) {
     const int ldq = D + F;
     const int ldy = D + 2 * dkv + 2 * F;
-    const int ok = D, ov = D + dkv, og = D + 2 * dkv, ou = og + F;
+    const int ok = D, og = D + 2 * dkv, ou = og + F;   // v follows k directly
     const int per_row = D / 8 + (2 * dkv) / 8 + F / 8;
     const int64_t total = (int64_t)M * per_row;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

@@ -31,8 +31,6 @@ using namespace lsn;
 namespace {
 
 inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
-inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
-inline int tiles_of(int64_t m, int64_t n, int bn) { return pair_tiles(m, n, bn); }
 
 struct Dims {
     int L, D, dkv, F, r, M, Ncat;
@@ -212,8 +210,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         GemmPlan g(c.dry);
         int mh = g.map(b.h[l], M, D, D, kBM);
         int ma = g.map(c.A(lora, kQ), 5 * r, D, D, 64);
-        g.problem(M, 5 * r, 64, A_KMAJOR, EPI_BF16, b.tcat[l], 5 * r, 1.0f, 5 * r,
-                  choose_splits(tiles_of(M, 5 * r, 64), D / kBK));
+        g.problem(M, 5 * r, 64, A_KMAJOR, EPI_BF16, b.tcat[l], 5 * r, 1.0f, 5 * r, kAutoSplits);
         g.seg(mh, 0, B_TMA_K, ma, 0, 0, D);
         RC(c.run(g));
     }
@@ -221,13 +218,10 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         GemmPlan g(c.dry);
         int mh = g.map(b.h[l], M, D, D, kBM);
         int mt = g.map(b.tcat[l], M, 5 * r, 5 * r, kBM);
-        int tiles = 0;
-        for (int p = 0; p < 5; ++p) tiles += tiles_of(M, d.np[p], 256);
-        const int sp = choose_splits(tiles, D / kBK);
         for (int p = 0; p < 5; ++p) {
             int v = g.nf4(c.mat(img, p), d.np[p], D);
             g.problem(M, d.np[p], 256, A_KMAJOR, EPI_BF16, b.y[l] ? b.y[l] + d.coff[p] : nullptr, d.Ncat, 1.0f,
-                      d.np[p], sp);
+                      d.np[p], kAutoSplits);
             g.seg(mh, 0, B_NF4_K, v, 0, 0, D);
             g.seg_scaled(mt, p * r, c.B(lora, p), r, d.np[p], r, d.s);
         }
@@ -240,11 +234,9 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         int ma = g.map(b.a[l], M, d.F, d.F, kBM);
         int mao = g.map(c.A(lora, kO), r, D, D, 64);
         int mad = g.map(c.A(lora, kDown), r, d.F, d.F, 64);
-        const int tiles = 2 * tiles_of(M, r, 64);
-        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l], 2 * r, 1.0f, r, choose_splits(tiles, D / kBK));
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l], 2 * r, 1.0f, r, kAutoSplits);
         g.seg(mq, 0, B_TMA_K, mao, 0, 0, D);
-        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l] ? b.tod[l] + r : nullptr, 2 * r, 1.0f, r,
-                  choose_splits(tiles, d.F / kBK));
+        g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.tod[l] ? b.tod[l] + r : nullptr, 2 * r, 1.0f, r, kAutoSplits);
         g.seg(ma, 0, B_TMA_K, mad, 0, 0, d.F);
         RC(c.run(g));
     }
@@ -257,8 +249,7 @@ int fwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, bool reco
         int mt = g.map(b.tod[l], M, 2 * r, 2 * r, kBM);
         int vo = g.nf4(c.mat(img, kO), D, D);
         int vd = g.nf4(c.mat(img, kDown), D, d.F);
-        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, b.x[l + 1], D, 1.0f, D,
-                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK), b.x[l], D);
+        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, b.x[l + 1], D, 1.0f, D, kAutoSplits, b.x[l], D);
         g.seg(mq, 0, B_NF4_K, vo, 0, 0, D);
         g.seg(ma, 0, B_NF4_K, vd, 0, 0, d.F);
         g.seg_scaled(mt, 0, c.B(lora, kO), r, D, r, d.s);
@@ -282,13 +273,10 @@ int ref_layer(Ctx& c, const uint8_t* img, const uint16_t* xin, uint16_t* xout) {
     {
         GemmPlan g(c.dry);
         int mh = g.map(b.hr, M, D, D, kBM);
-        int tiles = 0;
-        for (int p = 0; p < 5; ++p) tiles += tiles_of(M, d.np[p], 256);
-        const int sp = choose_splits(tiles, D / kBK);
         for (int p = 0; p < 5; ++p) {
             int v = g.nf4(c.mat(img, p), d.np[p], D);
             g.problem(M, d.np[p], 256, A_KMAJOR, EPI_BF16, b.yr ? b.yr + d.coff[p] : nullptr, d.Ncat, 1.0f, d.np[p],
-                      sp);
+                      kAutoSplits);
             g.seg(mh, 0, B_NF4_K, v, 0, 0, D);
         }
         RC(c.run(g));
@@ -300,8 +288,7 @@ int ref_layer(Ctx& c, const uint8_t* img, const uint16_t* xin, uint16_t* xout) {
         int ma = g.map(b.ar, M, d.F, d.F, kBM);
         int vo = g.nf4(c.mat(img, kO), D, D);
         int vd = g.nf4(c.mat(img, kDown), D, d.F);
-        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, xout, D, 1.0f, D,
-                  choose_splits(tiles_of(M, D, 256), (D + d.F) / kBK), xin, D);
+        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, xout, D, 1.0f, D, kAutoSplits, xin, D);
         g.seg(mq, 0, B_NF4_K, vo, 0, 0, D);
         g.seg(ma, 0, B_NF4_K, vd, 0, 0, d.F);
         RC(c.run(g));
@@ -321,7 +308,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         int mdx = g.map(b.dx_bf, M, D, D, kBM);
         int mbo = g.map(c.B(lora, kO), D, r, r, 64);
         int mbd = g.map(c.B(lora, kDown), D, r, r, 64);
-        const int sp = choose_splits(2 * tiles_of(M, r, 64), D / kBK);
+        const int sp = kAutoSplits;
         g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtod, 2 * r, d.s, r, sp);
         g.seg(mdx, 0, B_TMA_MN, mbo, 0, 0, D);
         g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtod ? b.dtod + r : nullptr, 2 * r, d.s, r, sp);
@@ -341,9 +328,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         int mad = g.map(c.A(lora, kDown), r, F, F, 64);
         int vo = g.nf4(c.mat(img, kO), D, D);
         int vd = g.nf4(c.mat(img, kDown), D, F);
-        const int tiles = 3 * tiles_of(D, r, 64) + tiles_of(F, r, 64) + tiles_of(M, D, 256) + tiles_of(M, F, 256);
-        const int ws = choose_splits(tiles, ceil_div(M, kBK));
-        const int xs = choose_splits(tiles, D / kBK);
+        const int ws = kAutoSplits, xs = kAutoSplits;
         g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kO), r, d.s, r, ws);
         g.seg(mdx_mn, 0, B_TMA_MN, mtod_mn, 0, 0, M);
         g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kDown), r, d.s, r, ws);
@@ -367,11 +352,9 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
     {   // dT_p = bf16(s dY_p B_p)
         GemmPlan g(c.dry);
         int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
-        int tiles = 5 * tiles_of(M, r, 64);
         for (int p = 0; p < 5; ++p) {
             int mb = g.map(c.B(lora, p), d.np[p], r, r, 64);
-            g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtcat ? b.dtcat + p * r : nullptr, 5 * r, d.s, r,
-                      choose_splits(tiles, ceil_div(d.np[p], kBK)));
+            g.problem(M, r, 64, A_KMAJOR, EPI_BF16, b.dtcat ? b.dtcat + p * r : nullptr, 5 * r, d.s, r, kAutoSplits);
             g.seg(mdy, d.coff[p], B_TMA_MN, mb, 0, 0, d.np[p]);
         }
         RC(c.run(g));
@@ -386,9 +369,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
         int mdtcat = g.map(b.dtcat, M, 5 * r, 5 * r, kBM);
         int macat = g.map(c.A(lora, kQ), 5 * r, D, D, 64);
-        int tiles = 5 * tiles_of(D, r, 64) + tiles_of(M, D, 256);
-        for (int p = 0; p < 5; ++p) tiles += tiles_of(d.np[p], r, 64);
-        const int ws = choose_splits(tiles, ceil_div(M, kBK));
+        const int ws = kAutoSplits;
         for (int p = 0; p < 5; ++p) {
             g.problem(d.np[p], r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, p), r, d.s, r, ws);
             g.seg(mdyp[p], 0, B_TMA_MN, mtcat_mn, 0, p * r, M);
@@ -397,9 +378,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
             g.problem(D, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, p), D, 1.0f, r, ws);
             g.seg(mh_mn, 0, B_TMA_MN, mdtcat_mn, 0, p * r, M);
         }
-        int ksteps = 0;
-        for (int p = 0; p < 5; ++p) ksteps += ceil_div(d.np[p], kBK);
-        g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dh, D, 1.0f, D, choose_splits(tiles, ksteps));
+        g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dh, D, 1.0f, D, kAutoSplits);
         for (int p = 0; p < 5; ++p) {
             int v = g.nf4(c.mat(img, p), d.np[p], D);
             g.seg(mdy, d.coff[p], B_NF4_MN, v, 0, 0, d.np[p]);

@@ -13,56 +13,89 @@ namespace lsn {
 
 static inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 static inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-static inline int tiles_of(int64_t m, int64_t n, int bn) { return pair_tiles(m, n, bn); }
 static inline int bn_for(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
-static inline int ksteps_of(int64_t k) { return (int)((k + kBK - 1) / kBK); }
 
 struct LinearShape {
     int64_t M, N, K;
     int r;
 };
 
-// Split counts used by the forward / backward launches (shared with the workspace query).
-struct FwdSplits { int t, y; };
-struct BwdSplits { int dt, db, da, dx; };
-
-// The LoRA k-steps of the Y launch are a tail (they go to the last split), so the splits
-// divide the base contraction only: the adapter-disabled launch splits it the same way.
-static FwdSplits fwd_splits(const LinearShape& s) {
-    FwdSplits f;
-    f.t = choose_splits(tiles_of(s.M, s.r, 64), ksteps_of(s.K));
-    f.y = choose_splits(tiles_of(s.M, s.N, bn_for(s.N)), ksteps_of(s.K));
-    return f;
+// The launches of the single linear, as plans.  Given null pointers and a dry plan they size
+// the workspace with exactly the split decisions of the real launch (the split planner sees
+// the same problems).  The LoRA k-steps of the Y launch are a tail: the adapter-disabled
+// launch splits the base contraction the same way.
+static void plan_fwd_T(GemmPlan& g, const LinearShape& s, const uint16_t* X, const uint16_t* A, uint16_t* T) {
+    const int K = (int)s.K;
+    int mx = g.map(X, s.M, K, K, kBM);
+    int ma = g.map(A, s.r, K, K, 64);
+    g.problem((int)s.M, s.r, 64, A_KMAJOR, EPI_BF16, T, s.r, 1.0f, s.r, kAutoSplits);
+    g.seg(mx, 0, B_TMA_K, ma, 0, 0, K);
 }
 
-LinearFwdSplits linear_fwd_splits(int64_t M, int64_t n_out, int64_t k_in, int r) {
-    const FwdSplits f = fwd_splits(LinearShape{M, n_out, k_in, r});
-    return LinearFwdSplits{f.t, f.y};
+static void plan_fwd_Y(GemmPlan& g, const LinearShape& s, const void* W, const uint16_t* X, const uint16_t* T,
+                       const uint16_t* B, float scale, const uint16_t* residual, uint16_t* Y, bool adapter) {
+    const int K = (int)s.K, N = (int)s.N;
+    int mx = g.map(X, s.M, K, K, kBM);
+    int wv = g.nf4(W, N, K);
+    g.problem((int)s.M, N, bn_for(N), A_KMAJOR, EPI_BF16, Y, N, 1.0f, N, kAutoSplits, residual, N);
+    g.seg(mx, 0, B_NF4_K, wv, 0, 0, K);
+    if (adapter) g.seg_scaled(g.map(T, s.M, s.r, s.r, kBM), 0, B, s.r, N, s.r, scale);
 }
 
-static BwdSplits bwd_splits(const LinearShape& s) {
-    BwdSplits b;
-    b.dt = choose_splits(tiles_of(s.M, s.r, 64), ksteps_of(s.N));
-    const int tiles2 = tiles_of(s.N, s.r, 64) + tiles_of(s.K, s.r, 64) + tiles_of(s.M, s.K, bn_for(s.K));
-    b.db = choose_splits(tiles2, ksteps_of(s.M));
-    b.da = b.db;
-    b.dx = choose_splits(tiles2, ksteps_of(s.N));
-    return b;
+static void plan_bwd_dT(GemmPlan& g, const LinearShape& s, const uint16_t* dY, const uint16_t* B, float scale,
+                        uint16_t* dT) {
+    const int N = (int)s.N;
+    int my = g.map(dY, s.M, N, N, kBM);
+    int mb = g.map(B, N, s.r, s.r, 64);
+    g.problem((int)s.M, s.r, 64, A_KMAJOR, EPI_BF16, dT, s.r, scale, s.r, kAutoSplits);
+    g.seg(my, 0, B_TMA_MN, mb, 0, 0, N);
 }
 
-static size_t partial_bytes(int splits, int64_t m, int64_t n) {
-    return splits > 1 ? align256((size_t)splits * m * n * sizeof(float)) : 0;
+// dB = s dY^T T ; dA^T = X^T dT ; dX (+)= dY W + dT A   (one grouped launch; dX optional)
+static void plan_bwd_main(GemmPlan& g, const LinearShape& s, const void* W, const uint16_t* X, const uint16_t* T,
+                          const uint16_t* dY, const uint16_t* A, const uint16_t* dT, float scale, float* dX,
+                          bool want_dX, bool accumulate_dX, float* dA, float* dB) {
+    const int K = (int)s.K, N = (int)s.N, m = (int)s.M, r = s.r;
+    int my_mn = g.map(dY, s.M, N, N, 64);
+    int mt_mn = g.map(T, s.M, r, r, 64);
+    int mx_mn = g.map(X, s.M, K, K, 64);
+    int mdt_mn = g.map(dT, s.M, r, r, 64);
+    g.problem(N, r, 64, A_MNMAJOR, EPI_F32, dB, r, scale, r, kAutoSplits);
+    g.seg(my_mn, 0, B_TMA_MN, mt_mn, 0, 0, m);
+    g.problem(K, r, 64, A_MNMAJOR, EPI_F32_T, dA, K, 1.0f, r, kAutoSplits);
+    g.seg(mx_mn, 0, B_TMA_MN, mdt_mn, 0, 0, m);
+    if (want_dX) {
+        int my = g.map(dY, s.M, N, N, kBM);
+        int mdt = g.map(dT, s.M, r, r, kBM);
+        int ma_mn = g.map(A, r, K, K, 64);
+        int wv = g.nf4(W, N, K);
+        g.problem(m, K, bn_for(K), A_KMAJOR, accumulate_dX ? EPI_F32_ACC : EPI_F32, dX, K, 1.0f, K, kAutoSplits);
+        g.seg(my, 0, B_NF4_MN, wv, 0, 0, N);
+        g.seg(mdt, 0, B_TMA_MN, ma_mn, 0, 0, r, true);
+    }
 }
 
-static size_t fwd_ws(const LinearShape& s) {
-    FwdSplits f = fwd_splits(s);
-    return partial_bytes(f.t, s.M, s.r) + partial_bytes(f.y, s.M, s.N);
+// Workspace of the forward: the T launch's partial slabs, then the Y launch's.
+struct FwdWs { size_t t, y; };
+static FwdWs fwd_ws(const LinearShape& s) {
+    GemmPlan gt(true), gy(true);
+    plan_fwd_T(gt, s, nullptr, nullptr, nullptr);
+    plan_fwd_Y(gy, s, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, nullptr, true);
+    return FwdWs{align256(gt.partial_bytes()), align256(gy.partial_bytes())};
 }
 
-static size_t bwd_ws(const LinearShape& s) {
-    BwdSplits b = bwd_splits(s);
-    return align256((size_t)s.M * s.r * 2) + partial_bytes(b.dt, s.M, s.r) + partial_bytes(b.db, s.N, s.r) +
-           partial_bytes(b.da, s.K, s.r) + partial_bytes(b.dx, s.M, s.K);
+// Workspace of the backward: dT (bf16 [M x r]), the dT launch's partials, the main launch's
+// partials (with or without dX, whichever needs more).
+struct BwdWs { size_t dt_out, dt, main; };
+static BwdWs bwd_ws(const LinearShape& s) {
+    GemmPlan g1(true), g2(true), g3(true);
+    plan_bwd_dT(g1, s, nullptr, nullptr, 1.0f, nullptr);
+    plan_bwd_main(g2, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, true, false, nullptr,
+                  nullptr);
+    plan_bwd_main(g3, s, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, false, false, nullptr,
+                  nullptr);
+    const size_t a = g2.partial_bytes(), b = g3.partial_bytes();
+    return BwdWs{align256((size_t)s.M * s.r * 2), align256(g1.partial_bytes()), align256(a > b ? a : b)};
 }
 
 static int check_linear(const nf4_view* W, int64_t M, int r, const void* X) {
@@ -73,6 +106,14 @@ static int check_linear(const nf4_view* W, int64_t M, int r, const void* X) {
     if (M < 1 || M > (1 << 30)) return fail(LSN_EINVAL, "lora: bad M");
     if (!al16(W->base) || !al16(X)) return fail(LSN_EINVAL, "lora: pointers must be 16-byte aligned");
     return LSN_OK;
+}
+
+int plan_linear_fwd(GemmPlan* gt, GemmPlan* gy, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,
+                    const uint16_t* B, int r, float scale, const uint16_t* residual, uint16_t* Y, uint16_t* T_out) {
+    const LinearShape s{M, W->n_out, W->k_in, r};
+    plan_fwd_T(*gt, s, X, A, T_out);
+    plan_fwd_Y(*gy, s, W->base, X, T_out, B, scale, residual, Y, true);
+    return gt->status() ? gt->status() : gy->status();
 }
 
 int check_linear_fwd(const char* who, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,
@@ -97,10 +138,29 @@ using namespace lsn;
 extern "C" {
 
 size_t lora_nf4_workspace_bytes(int64_t M, int64_t n_out, int64_t k_in, int r) {
-    if (M < 1 || n_out < 1 || k_in < 64 || r < 8 || r > 64) return 0;
-    LinearShape s{M, n_out, k_in, r};
-    size_t a = fwd_ws(s), b = bwd_ws(s);
-    return (a > b ? a : b) + 256;
+    if (M < 1 || M > (1 << 30) || n_out < 8 || n_out % 8 || k_in < 64 || k_in % 64 || r < 8 || r > 64 || r % 8)
+        return 0;
+    const LinearShape s{M, n_out, k_in, r};
+    const FwdWs f = fwd_ws(s);
+    const BwdWs b = bwd_ws(s);
+    const size_t a = f.t + f.y, c = b.dt_out + b.dt + b.main;
+    return (a > c ? a : c) + 256;
+}
+
+int lora_nf4_fwd_plan(int64_t M, int64_t n_out, int64_t k_in, int r, int* t_splits, int* y_splits,
+                      size_t* t_partial_bytes, size_t* y_partial_bytes) {
+    if (M < 1 || M > (1 << 30) || n_out < 8 || n_out % 8 || k_in < 64 || k_in % 64 || r < 8 || r > 64 || r % 8)
+        return fail(LSN_EINVAL, "lora_nf4_fwd_plan: shape refused by lora_nf4_fwd");
+    const LinearShape s{M, n_out, k_in, r};
+    GemmPlan gt(true), gy(true);
+    plan_fwd_T(gt, s, nullptr, nullptr, nullptr);
+    plan_fwd_Y(gy, s, nullptr, nullptr, nullptr, nullptr, 1.0f, nullptr, nullptr, true);
+    if (gt.status() || gy.status()) return gt.status() ? gt.status() : gy.status();
+    if (t_splits) *t_splits = gt.splits_of(0);
+    if (y_splits) *y_splits = gy.splits_of(0);
+    if (t_partial_bytes) *t_partial_bytes = gt.partial_bytes();
+    if (y_partial_bytes) *y_partial_bytes = gy.partial_bytes();
+    return LSN_OK;
 }
 
 int nf4_dequant(const nf4_view* W, uint16_t* out, void* stream) {
@@ -127,32 +187,21 @@ int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t
     int rc = check_linear_fwd("lora_nf4_fwd", W, X, M, A, B, r, residual, Y, T_out, adapter);
     if (rc) return rc;
     const LinearShape s{M, W->n_out, W->k_in, r};
-    if (ws_bytes < fwd_ws(s) || (fwd_ws(s) && !ws))
-        return fail(LSN_ENOMEM, "lora_nf4_fwd: workspace %zu < %zu", ws_bytes, fwd_ws(s));
+    const FwdWs f = fwd_ws(s);
+    if (ws_bytes < f.t + f.y || (f.t + f.y && !ws))
+        return fail(LSN_ENOMEM, "lora_nf4_fwd: workspace %zu < %zu", ws_bytes, f.t + f.y);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const FwdSplits f = fwd_splits(s);
-    const int K = (int)s.K, N = (int)s.N, m = (int)M;
-
-    // T = bf16(X A^T)
-    if (adapter) {
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    if (adapter) {   // T = bf16(X A^T)
         GemmPlan g;
-        int mx = g.map(X, M, K, K, kBM);
-        int ma = g.map(A, r, K, K, 64);
-        g.problem(m, r, 64, A_KMAJOR, EPI_BF16, T_out, r, 1.0f, r, f.t);
-        g.seg(mx, 0, B_TMA_K, ma, 0, 0, K);
-        rc = g.launch(st, static_cast<float*>(ws), ws_bytes);
+        plan_fwd_T(g, s, X, A, T_out);
+        rc = g.launch(st, reinterpret_cast<float*>(wsb), f.t);
         if (rc) return rc;
     }
-    // Y = bf16(X W^T + s T B^T [+ residual])
-    {
-        uint8_t* wsb = static_cast<uint8_t*>(ws) + partial_bytes(f.t, s.M, s.r);
+    {   // Y = bf16(X W^T + s T B^T [+ residual])
         GemmPlan g;
-        int mx = g.map(X, M, K, K, kBM);
-        int wv = g.nf4(W->base, N, K);
-        g.problem(m, N, bn_for(N), A_KMAJOR, EPI_BF16, Y, N, 1.0f, N, f.y, residual, N);
-        g.seg(mx, 0, B_NF4_K, wv, 0, 0, K);
-        if (adapter) g.seg_scaled(g.map(T_out, M, r, r, kBM), 0, B, r, N, r, scale);
-        rc = g.launch(st, reinterpret_cast<float*>(wsb), ws_bytes - (wsb - static_cast<uint8_t*>(ws)));
+        plan_fwd_Y(g, s, W->base, X, T_out, B, scale, residual, Y, adapter);
+        rc = g.launch(st, reinterpret_cast<float*>(wsb ? wsb + f.t : nullptr), ws_bytes - f.t);
         if (rc) return rc;
     }
     return LSN_OK;
@@ -167,47 +216,22 @@ int lora_nf4_bwd(const nf4_view* W, const uint16_t* X, const uint16_t* T, const 
     if (!al16(T) || !al16(dY) || !al16(A) || !al16(B) || !al16(dA) || !al16(dB) || (dX && !al16(dX)))
         return fail(LSN_EINVAL, "lora_nf4_bwd: pointers must be 16-byte aligned");
     const LinearShape s{M, W->n_out, W->k_in, r};
-    if (ws_bytes < bwd_ws(s) || !ws)
-        return fail(LSN_ENOMEM, "lora_nf4_bwd: workspace %zu < %zu", ws_bytes, bwd_ws(s));
+    const BwdWs b = bwd_ws(s);
+    const size_t need = b.dt_out + b.dt + b.main;
+    if (ws_bytes < need || !ws) return fail(LSN_ENOMEM, "lora_nf4_bwd: workspace %zu < %zu", ws_bytes, need);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const BwdSplits b = bwd_splits(s);
-    const int K = (int)s.K, N = (int)s.N, m = (int)M;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     uint16_t* dT = reinterpret_cast<uint16_t*>(wsb);
-    size_t off = align256((size_t)M * r * 2);
-
-    // dT = bf16(s dY B)
-    {
+    {   // dT = bf16(s dY B)
         GemmPlan g;
-        int my = g.map(dY, M, N, N, kBM);
-        int mb = g.map(B, N, r, r, 64);
-        g.problem(m, r, 64, A_KMAJOR, EPI_BF16, dT, r, scale, r, b.dt);
-        g.seg(my, 0, B_TMA_MN, mb, 0, 0, N);
-        rc = g.launch(st, reinterpret_cast<float*>(wsb + off), ws_bytes - off);
+        plan_bwd_dT(g, s, dY, B, scale, dT);
+        rc = g.launch(st, reinterpret_cast<float*>(wsb + b.dt_out), b.dt);
         if (rc) return rc;
-        off += partial_bytes(b.dt, s.M, s.r);
     }
-    // dB = s dY^T T ; dA^T = X^T dT ; dX (+)= dY W + dT A   (one grouped launch)
-    {
+    {   // dB, dA and dX in one grouped launch
         GemmPlan g;
-        int my_mn = g.map(dY, M, N, N, 64);
-        int mt_mn = g.map(T, M, r, r, 64);
-        int mx_mn = g.map(X, M, K, K, 64);
-        int mdt_mn = g.map(dT, M, r, r, 64);
-        g.problem(N, r, 64, A_MNMAJOR, EPI_F32, dB, r, scale, r, b.db);
-        g.seg(my_mn, 0, B_TMA_MN, mt_mn, 0, 0, m);
-        g.problem(K, r, 64, A_MNMAJOR, EPI_F32_T, dA, K, 1.0f, r, b.da);
-        g.seg(mx_mn, 0, B_TMA_MN, mdt_mn, 0, 0, m);
-        if (dX) {
-            int my = g.map(dY, M, N, N, kBM);
-            int mdt = g.map(dT, M, r, r, kBM);
-            int ma_mn = g.map(A, r, K, K, 64);
-            int wv = g.nf4(W->base, N, K);
-            g.problem(m, K, bn_for(K), A_KMAJOR, accumulate_dX ? EPI_F32_ACC : EPI_F32, dX, K, 1.0f, K, b.dx);
-            g.seg(my, 0, B_NF4_MN, wv, 0, 0, N);
-            g.seg(mdt, 0, B_TMA_MN, ma_mn, 0, 0, r, true);
-        }
-        rc = g.launch(st, reinterpret_cast<float*>(wsb + off), ws_bytes - off);
+        plan_bwd_main(g, s, W->base, X, T, dY, A, dT, scale, dX, dX != nullptr, accumulate_dX != 0, dA, dB);
+        rc = g.launch(st, reinterpret_cast<float*>(wsb + b.dt_out + b.dt), b.main);
         if (rc) return rc;
     }
     return LSN_OK;

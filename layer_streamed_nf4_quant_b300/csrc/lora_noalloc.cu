@@ -62,10 +62,6 @@ int static_addresses(StaticAddrs* out) {
     return LSN_OK;
 }
 
-inline size_t partial_bytes(int splits, int64_t m, int64_t n) {
-    return splits > 1 ? (size_t)splits * (size_t)m * (size_t)n * sizeof(float) : 0;
-}
-
 }  // namespace
 
 int static_error_take(uint32_t* v) {
@@ -95,12 +91,11 @@ extern "C" int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X,
     // the same checks (shapes, NULLs, 16-byte alignment of every pointer) as lora_nf4_fwd
     int rc = check_linear_fwd("lora_nf4_fwd_static_scratch", W, X, M, A, B, r, residual, Y, T_out, true);
     if (rc) return rc;
-    const int K = (int)W->k_in, N = (int)W->n_out, m = (int)M;
-    // the same split decisions as lora_nf4_fwd, so both give the same bits
-    const int bn = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-    const LinearFwdSplits sp = linear_fwd_splits(M, N, K, r);
-    const int st = sp.t, sy = sp.y;
-    const size_t need_t = partial_bytes(st, M, r), need_y = partial_bytes(sy, M, N);
+    // the same plans (and so the same split decisions) as lora_nf4_fwd, so both give the same bits
+    GemmPlan gt, gy;
+    rc = plan_linear_fwd(&gt, &gy, W, X, M, A, B, r, scale, residual, Y, T_out);
+    if (rc) return rc;
+    const size_t need_t = gt.partial_bytes(), need_y = gy.partial_bytes();
     const size_t need = need_t > need_y ? need_t : need_y;
     if (need > kStaticScratchBytes)
         return fail(LSN_ENOMEM,
@@ -112,28 +107,12 @@ extern "C" int lora_nf4_fwd_static_scratch(const nf4_view* W, const uint16_t* X,
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* scratch = static_cast<float*>(sa.scratch);
-    {   // T = bf16(X A^T)
-        GemmPlan g;
-        g.set_error_word(sa.err);
-        int mx = g.map(X, M, K, K, kBM);
-        int ma = g.map(A, r, K, K, 64);
-        g.problem(m, r, 64, A_KMAJOR, EPI_BF16, T_out, r, 1.0f, r, st);
-        g.seg(mx, 0, B_TMA_K, ma, 0, 0, K);
-        rc = g.launch(s, scratch, kStaticScratchBytes);
-        if (rc) return rc;
-    }
-    {   // Y = bf16(X W^T + s T B^T [+ residual])
-        GemmPlan g;
-        g.set_error_word(sa.err);
-        int mx = g.map(X, M, K, K, kBM);
-        int mt = g.map(T_out, M, r, r, kBM);
-        int wv = g.nf4(W->base, N, K);
-        g.problem(m, N, bn, A_KMAJOR, EPI_BF16, Y, N, 1.0f, N, sy, residual, N);
-        g.seg(mx, 0, B_NF4_K, wv, 0, 0, K);
-        g.seg_scaled(mt, 0, B, r, N, r, scale);
-        rc = g.launch(s, scratch, kStaticScratchBytes);
-        if (rc) return rc;
-    }
+    gt.set_error_word(sa.err);   // T = bf16(X A^T)
+    rc = gt.launch(s, scratch, kStaticScratchBytes);
+    if (rc) return rc;
+    gy.set_error_word(sa.err);   // Y = bf16(X W^T + s T B^T [+ residual])
+    rc = gy.launch(s, scratch, kStaticScratchBytes);
+    if (rc) return rc;
     if (device_status) {
         // synchronous status read: wait for this call's kernels, read and clear the word
         LSN_CUDA_TRY(cudaStreamSynchronize(s));

@@ -28,12 +28,12 @@ enum DeviceErrorKind : uint32_t {
     kDevErrTag = 2u,       // layer image tag mismatch (detail: expected layer)
 };
 
-// Split counts of the single-linear forward (the T launch and the Y launch).  Shared by
-// lora_nf4_fwd and lora_nf4_fwd_static_scratch, so the two give the same bits.
-struct LinearFwdSplits {
-    int t, y;
-};
-LinearFwdSplits linear_fwd_splits(int64_t M, int64_t n_out, int64_t k_in, int r);
+class GemmPlan;
+// The two launches of the single-linear forward (T, then Y) as plans, exactly as
+// lora_nf4_fwd builds them: lora_nf4_fwd_static_scratch uses them, so the two give the same
+// bits.  Returns the plans' status.
+int plan_linear_fwd(GemmPlan* gt, GemmPlan* gy, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,
+                    const uint16_t* B, int r, float scale, const uint16_t* residual, uint16_t* Y, uint16_t* T_out);
 // Argument checks of the single-linear forward entry points (shapes, NULLs, 16-byte
 // alignment of every operand and output).  adapter == false: A, B and T_out are not used.
 int check_linear_fwd(const char* who, const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A,

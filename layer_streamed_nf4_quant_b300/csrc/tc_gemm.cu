@@ -24,6 +24,10 @@
 #include <cuda_bf16.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
+#include <vector>
+
 #include "lsn_internal.h"
 #include "tc_gemm.h"
 #include "tc_ptx.cuh"
@@ -286,38 +290,21 @@ __device__ __forceinline__ DeqJob make_deq_job(const GemmParams& p, const SeqPos
 
 // ----------------------------------------------------------------------------- epilogue
 
-// Epilogue of one warp: its 32 accumulator rows (lane = row row0 + lane) in chunks of 32
-// columns.  bf16 and fp32 outputs go through two alternating 4 KB staging tiles in shared
-// memory (128-byte rows, 16-byte pieces XOR-swizzled by row, the layout of a 128-byte
-// swizzled TMA box) and leave by bulk tensor stores: 64 columns per bf16 tile, 32 per fp32
-// tile.  The stores run in the background, so the accumulator is released as soon as its
-// last chunk is in registers.  The arithmetic per element is alpha * acc, then the residual
-// (bf16) or, for EPI_F32_ACC, the old value added by the bulk reduce (one fp32 addition,
-// commutative), then the rounding.
+// Epilogue of one warp: its 32 accumulator rows (lane = row row0 + lane), 128 bytes of each
+// row per step (64 bf16 or 32 fp32 columns).  Each step writes the values row by row into one
+// of the warp's two 4 KB staging tiles in shared memory (16-byte pieces XOR-swizzled by row,
+// so neither the row-wise writes nor the column-wise reads conflict), then reads the tile
+// back so that every 8 lanes hold one 128-byte row segment and store it with st.global.v4:
+// coalesced, with no bulk-copy unit, proxy fence or completion wait on the path (the bulk
+// tensor stores this replaces shared the copy unit with the A loads and waited for it).  The
+// two tiles alternate, so one __syncwarp per step orders a tile's writes before its reads and
+// its reads before its next writes.  The arithmetic per element: alpha * acc, then the
+// residual (bf16 outputs) or, for EPI_F32_ACC, the old value of the output (one fp32
+// addition per element), then the rounding.
 struct EpiStage {
     uint32_t base;   // this warp's two staging tiles
     uint32_t buf;    // the tile written next
 };
-
-__device__ __forceinline__ void epi_acquire(EpiStage& st, int lane) {
-    if (lane == 0) ptx::bulk_wait_read_1();   // the tile written two stores ago has been read
-    __syncwarp();
-}
-
-__device__ __forceinline__ void epi_release(EpiStage& st, int lane, const CUtensorMap* map, int mode,
-                                           int x, int y, int z) {
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        const uint32_t src = st.base + st.buf * kEpiStageBytes;
-        if (mode == EPI_PARTIAL) ptx::tma_store_3d(map, src, x, y, z);
-        else if (mode == EPI_F32_ACC) ptx::tma_reduce_add_2d(map, src, x, y);
-        else ptx::tma_store_2d_hint(map, src, x, y, ptx::policy_evict_first());   // not read again here
-        ptx::bulk_commit();
-    }
-    __syncwarp();
-    st.buf ^= 1u;
-}
 
 // The per-problem values the epilogue needs, copied into registers once per tile.
 struct EpiArgs {
@@ -325,6 +312,7 @@ struct EpiArgs {
     float alpha;
     void* out;
     int64_t ldo;
+    int64_t part_stride;
     const uint16_t* residual;
     int64_t ldr;
 };
@@ -338,13 +326,67 @@ __device__ __forceinline__ EpiArgs epi_args(const Problem& pr, int split) {
     a.alpha = pr.alpha;
     a.out = pr.out;
     a.ldo = pr.ldo;
+    a.part_stride = pr.part_stride;
     a.residual = pr.residual;
     a.ldr = pr.ldr;
     return a;
 }
 
-__device__ __forceinline__ void epi_chunk(const EpiArgs& a, const CUtensorMap* map, int row0, int col0,
-                                          const uint32_t (&r)[32], EpiStage& st, int lane) {
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// Output stores are not read again by this kernel: evict-first keeps L2 for the A rows.
+__device__ __forceinline__ void st_global_v4_ef(void* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
+// One step: w = this lane's 128 bytes of row row0 + lane (kElemBytes per element), written
+// to the output columns col0 .. col0 + 128 / kElemBytes.
+template <int kElemBytes>
+__device__ __forceinline__ void epi_flush(const EpiArgs& a, int row0, int col0, const uint32_t (&w)[32], EpiStage& st,
+                                          int lane, uint64_t pol) {
+    const uint32_t tile = st.base + st.buf * kEpiStageBytes;
+    const uint32_t swz = (uint32_t)(lane & 7);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        st_shared_v4(tile + (uint32_t)lane * 128u + ((((uint32_t)g) ^ swz) << 4), w[4 * g], w[4 * g + 1],
+                     w[4 * g + 2], w[4 * g + 3]);
+    __syncwarp();
+    constexpr int kPer16 = 16 / kElemBytes;   // elements per 16-byte piece
+    const int c = lane & 7;                   // this lane's piece of each row segment
+    const int col = col0 + c * kPer16;
+    const bool col_ok = col < a.n_valid;      // n_valid is a multiple of 8: pieces are whole
+    char* base = static_cast<char*>(a.out);
+    if (a.epi == EPI_PARTIAL) base += (int64_t)a.split * a.part_stride * 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3);
+        const int row = row0 + r;
+        uint4 v = ld_shared_v4(tile + (uint32_t)r * 128u + ((((uint32_t)c) ^ (uint32_t)(r & 7)) << 4));
+        if (row < a.m && col_ok) {
+            void* o = base + ((int64_t)row * a.ldo + col) * kElemBytes;
+            if (kElemBytes == 4 && a.epi == EPI_F32_ACC) {
+                const float4 old = *reinterpret_cast<const float4*>(o);
+                v.x = __float_as_uint(old.x + __uint_as_float(v.x));
+                v.y = __float_as_uint(old.y + __uint_as_float(v.y));
+                v.z = __float_as_uint(old.z + __uint_as_float(v.z));
+                v.w = __float_as_uint(old.w + __uint_as_float(v.w));
+            }
+            st_global_v4_ef(o, v, pol);
+        }
+    }
+    st.buf ^= 1u;
+}
+
+// fp32 outputs, 32 columns per step (EPI_F32, EPI_F32_ACC, EPI_PARTIAL; EPI_F32_T is written
+// directly, transposed).
+__device__ __forceinline__ void epi_chunk(const EpiArgs& a, int row0, int col0, const uint32_t (&r)[32], EpiStage& st,
+                                          int lane, uint64_t pol) {
     const float al = a.alpha;
     if (a.epi == EPI_F32_T) {
         // transposed output: for a fixed column the lanes write consecutive rows
@@ -358,63 +400,18 @@ __device__ __forceinline__ void epi_chunk(const EpiArgs& a, const CUtensorMap* m
         __syncwarp();
         return;
     }
-    const uint32_t swz = (uint32_t)(lane & 7);
-    if (a.epi == EPI_BF16) {
-        const int half = (col0 >> 5) & 1;   // which 32 columns of the 64-column tile
-        const int tcol = col0 - 32 * half;
-        // warp-uniform: a second half wholly past the valid columns was left out when the
-        // tile was stored after its first half
-        if (col0 >= a.n_valid) return;
-        if (half == 0) epi_acquire(st, lane);
-        const int row = row0 + lane;
-        const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
-        const bool res_row = a.residual != nullptr && row < a.m;
-        const bool unit = al == 1.0f;   // x * 1.0f == x exactly, so the multiply is skipped
-        const uint16_t* rp = res_row ? a.residual + (int64_t)row * a.ldr + col0 : nullptr;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            float f[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = unit ? __uint_as_float(r[8 * g + j]) : __uint_as_float(r[8 * g + j]) * al;
-            if (res_row && col0 + 8 * g < a.n_valid) {
-                const uint4 r4 = *reinterpret_cast<const uint4*>(rp + 8 * g);
-                const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    f[2 * j] += __uint_as_float(rw[j] << 16);
-                    f[2 * j + 1] += __uint_as_float(rw[j] & 0xFFFF0000u);
-                }
-            }
-            st_shared_v4(dst + ((((uint32_t)(4 * half + g)) ^ swz) << 4), pack_bf16x2(f[0], f[1]),
-                         pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-        }
-        // the tile leaves after its second half, or after the first when the second half
-        // lies wholly past the valid columns (the box is clipped there anyway)
-        if (half == 1 || col0 + 32 >= a.n_valid) epi_release(st, lane, map, EPI_BF16, tcol, row0, 0);
-        else __syncwarp();
-        return;
-    }
     if (col0 >= a.n_valid) return;   // warp-uniform
-    epi_acquire(st, lane);
     const float a2 = a.epi == EPI_PARTIAL ? 1.0f : al;
-    const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
+    uint32_t w[32];
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
-        st_shared_v4(dst + ((((uint32_t)g) ^ swz) << 4), __float_as_uint(__uint_as_float(r[4 * g]) * a2),
-                     __float_as_uint(__uint_as_float(r[4 * g + 1]) * a2),
-                     __float_as_uint(__uint_as_float(r[4 * g + 2]) * a2),
-                     __float_as_uint(__uint_as_float(r[4 * g + 3]) * a2));
-    epi_release(st, lane, map, a.epi, col0, row0, a.split);
+    for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(r[j]) * a2);
+    epi_flush<4>(a, row0, col0, w, st, lane, pol);
 }
 
-// bf16 output, two chunks (64 columns, one staging tile) at once: all 32 packed words are
-// computed before the shared-memory stores, so the two halves' conversions overlap; one
-// fence and one bulk store per tile.  Same arithmetic as epi_chunk.
-__device__ __forceinline__ void epi_pair_bf16(const EpiArgs& a, const CUtensorMap* map, int row0, int col0,
-                                              const uint32_t (&ra)[32], const uint32_t (&rb)[32], EpiStage& st,
-                                              int lane) {
+// bf16 output, 64 columns (two 32-column accumulator chunks) per step.
+__device__ __forceinline__ void epi_pair_bf16(const EpiArgs& a, int row0, int col0, const uint32_t (&ra)[32],
+                                              const uint32_t (&rb)[32], EpiStage& st, int lane, uint64_t pol) {
     if (col0 >= a.n_valid) return;   // warp-uniform
-    epi_acquire(st, lane);
     const float al = a.alpha;
     const bool unit = al == 1.0f;   // x * 1.0f == x exactly, so the multiply is skipped
     const int row = row0 + lane;
@@ -440,12 +437,7 @@ __device__ __forceinline__ void epi_pair_bf16(const EpiArgs& a, const CUtensorMa
 #pragma unroll
         for (int j = 0; j < 4; ++j) w[4 * g + j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
     }
-    const uint32_t dst = st.base + st.buf * kEpiStageBytes + (uint32_t)lane * 128u;
-    const uint32_t swz = (uint32_t)(lane & 7);
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-        st_shared_v4(dst + ((((uint32_t)g) ^ swz) << 4), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-    epi_release(st, lane, map, EPI_BF16, col0, row0, 0);
+    epi_flush<2>(a, row0, col0, w, st, lane, pol);
 }
 
 // ------------------------------------------------------------------------------ kernel
@@ -553,9 +545,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ pair UMMA issuer (rank 0)
+        // One thread issues every pair MMA, so its own instructions per k-step bound the
+        // tensor rate when the stages are ready (they nearly always are): the tile's k-steps
+        // are walked segment by segment with no parameter loads inside, and the stage
+        // barriers are polled with test_wait.
         if (lane == 0 && leader) {
-            SeqPos s;
-            seq_begin(p, s, rank);
             uint32_t acc_phase = 0;
             uint32_t i = 0;
             // Operand descriptors at stage 0; the start-address field (address / 16, bits 0-13)
@@ -563,12 +557,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             const uint64_t dA_k = ptx::smem_desc_sw128(sA, 16, 1024), dA_mn = ptx::smem_desc_sw128(sA, 8192, 1024);
             const uint64_t dB_k = ptx::smem_desc_sw128(sB, 16, 1024), dB_mn = ptx::smem_desc_sw128(sB, 8192, 1024);
             constexpr uint32_t kHalfA16 = (kStageABytes / 2) >> 4;   // the second 128-row block
-            while (s.t < p.total_tiles) {
-                const int t = s.t;
-                const TileInfo ti = s.ti;
+            bool ok = true;
+            for (int t = (int)ptx::cluster_id_x(); ok && t < p.total_tiles; t += (int)ptx::n_clusters_x()) {
+                const TileInfo ti = decode_tile(p, t, rank);
                 const Problem& pr = p.probs[ti.prob];
-                if (!ptx::mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, p.err, kSiteAccEmpty))
-                    break;
+                if (!ptx::mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, p.err, kSiteAccEmpty)) break;
                 ptx::tc_fence_after();
                 const bool a_mn = pr.a_major == A_MNMAJOR;
                 const uint64_t dA = a_mn ? dA_mn : dA_k;
@@ -577,31 +570,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                 const uint32_t idesc_bmn = ptx::idesc_bf16_f32(pr.bn, a_mn ? 1 : 0, 1, 256);
                 const uint32_t tmem_h1 = tmem + (uint32_t)pr.bn;
                 const bool h0 = ti.half0, h1 = ti.half1;
-                bool ok = true;
-                for (; s.t == t; ++i, seq_next(p, s, rank)) {
-                    const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
-                    if (!ptx::mbar_wait_bounded_cta(full_bar(stage), phase, abort_flag, p.err, kSiteFull) ||
-                        !ptx::mbar_wait_bounded(pfull_bar(stage), phase, abort_flag, p.err, kSitePeerFull)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const bool b_mn = seg_b_mn(p.segs[s.si].b_src);
+                int si, kk;
+                locate(p, pr, ti.ks_begin, si, kk);
+                uint32_t acc = 0u;   // the tile's first MMA overwrites the accumulator
+                for (int ks = ti.ks_begin; ok && ks < ti.ks_end; ++si, kk = 0) {
+                    const bool b_mn = seg_b_mn(p.segs[si].b_src);
+                    const int seg_end = ks + (p.segs[si].ksteps - kk) < ti.ks_end ? ks + (p.segs[si].ksteps - kk)
+                                                                                   : ti.ks_end;
                     const uint32_t idesc = b_mn ? idesc_bmn : idesc_bk;
-                    const uint64_t a0 = dA + ((stage * (uint32_t)kStageABytes) >> 4);
-                    const uint64_t b0 = (b_mn ? dB_mn : dB_k) + ((stage * (uint32_t)kStageBBytes) >> 4);
+                    const uint64_t dB = b_mn ? dB_mn : dB_k;
                     const uint32_t b_k16 = b_mn ? (2048u >> 4) : (32u >> 4);
-                    const bool first = s.ks == ti.ks_begin;
+                    for (; ks < seg_end; ++ks, ++i) {
+                        const uint32_t stage = i % kStages, phase = (i / kStages) & 1u;
+                        if (!ptx::mbar_poll_bounded<false>(full_bar(stage), phase, abort_flag, p.err, kSiteFull) ||
+                            !ptx::mbar_poll_bounded<true>(pfull_bar(stage), phase, abort_flag, p.err, kSitePeerFull)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint64_t a0 = dA + ((stage * (uint32_t)kStageABytes) >> 4);
+                        const uint64_t b0 = dB + ((stage * (uint32_t)kStageBBytes) >> 4);
 #pragma unroll
-                    for (int k4 = 0; k4 < kBK / 16; ++k4) {
-                        // rows of block h: 128 of this CTA's tile and 128 of the peer's
-                        const uint64_t bd = b0 + (uint64_t)(k4 * b_k16);
-                        const uint64_t ad = a0 + (uint64_t)(k4 * a_k16);
-                        const uint32_t acc = (first && k4 == 0) ? 0u : 1u;
-                        if (h0) ptx::umma_f16_pair(tmem, ad, bd, idesc, acc);
-                        if (h1) ptx::umma_f16_pair(tmem_h1, ad + kHalfA16, bd, idesc, acc);
+                        for (int k4 = 0; k4 < kBK / 16; ++k4) {
+                            // rows of block h: 128 of this CTA's tile and 128 of the peer's
+                            const uint64_t bd = b0 + (uint64_t)(k4 * b_k16);
+                            const uint64_t ad = a0 + (uint64_t)(k4 * a_k16);
+                            if (h0) ptx::umma_f16_pair(tmem, ad, bd, idesc, acc);
+                            if (h1) ptx::umma_f16_pair(tmem_h1, ad + kHalfA16, bd, idesc, acc);
+                            acc = 1u;
+                        }
+                        ptx::umma_commit_pair_mc(empty_bar(stage), 0x3);
                     }
-                    ptx::umma_commit_pair_mc(empty_bar(stage), 0x3);
                 }
                 if (!ok) break;
                 ptx::umma_commit_pair_mc(acc_full, 0x3);
@@ -631,11 +630,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
         uint32_t acc_phase = 0;
         const uint32_t acc_empty_dst = leader ? acc_empty : ptx::mapa(acc_empty, 0);
         EpiStage est{sStg + (uint32_t)q * 2u * kEpiStageBytes, 0u};
+        const uint64_t pol_out = ptx::policy_evict_first();
         for (int t = (int)ptx::cluster_id_x(); t < p.total_tiles; t += (int)ptx::n_clusters_x()) {
             const TileInfo ti = decode_tile(p, t, rank);
             const TileInfo t0 = decode_tile(p, t, 0);   // which blocks the pair MMAs wrote
             const Problem& pr = p.probs[ti.prob];
-            const CUtensorMap* omap = &p.out_maps[ti.prob];
             const EpiArgs ea = epi_args(pr, ti.split);
             int ok = 0;
             if (lane == 0) ok = ptx::mbar_wait_bounded(acc_full, acc_phase, abort_flag, p.err, kSiteAccFull);
@@ -660,18 +659,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
                     ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
                     ptx::tmem_ld_wait(ra);
                     ptx::tmem_ld_wait(rb);
-                    epi_pair_bf16(ea, omap, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, rb, est, lane);
+                    epi_pair_bf16(ea, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, rb, est, lane, pol_out);
                 }
             } else {
             ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * pr.bn + chunk_c(0)), ra);
             ptx::tmem_ld_wait(ra);
             for (int i = 0; i < n_chunks; i += 2) {
                 if (i + 1 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
-                epi_chunk(ea, omap, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane);
+                epi_chunk(ea, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane, pol_out);
                 if (i + 1 >= n_chunks) break;
                 ptx::tmem_ld_wait(rb);
                 if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * pr.bn + chunk_c(i + 2)), ra);
-                epi_chunk(ea, omap, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est, lane);
+                epi_chunk(ea, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est, lane, pol_out);
                 if (i + 2 < n_chunks) ptx::tmem_ld_wait(ra);
             }
             }
@@ -680,9 +679,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             else ptx::mbar_arrive_remote(acc_empty_dst);
             acc_phase ^= 1u;
         }
-        // the bulk stores read shared memory and write the output: both end before the CTA does
-        if (lane == 0) ptx::bulk_wait_all();
-        __syncwarp();
     } else if (warp >= kDequantWarp0) {
         // --------------------------------------------------------------- B producer
         // Two groups of four warps take alternate k-steps of the sequence, so two k-steps
@@ -922,46 +918,142 @@ static int max_pair_clusters() {
     return n;
 }
 
-// Output tensor map of a problem for the bulk-store epilogue: bf16 boxes of 64 x 32, fp32
-// boxes of 32 x 32 (128-byte rows, 128-byte swizzle), clipped at m rows and n_valid columns;
-// split-K partials as a 3-D tensor [split][m][n] so that each split is clipped on its own.
-static int encode_out_map(const Problem& pr, CUtensorMap* map) {
-    if (pr.epi == EPI_F32_T) return LSN_OK;   // written directly
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return fail(LSN_ECUDA, "cuTensorMapEncodeTiled is unavailable");
-    const bool bf = pr.epi == EPI_BF16;
-    const int64_t es = bf ? 2 : 4;
-    if ((pr.ldo * es) % 16 || pr.ldo < pr.n_valid)
-        return fail(LSN_EINVAL, "gemm: output rows must be 16-byte multiples");
-    CUresult r;
-    if (pr.epi == EPI_PARTIAL) {
-        cuuint64_t dims[3] = {(cuuint64_t)pr.n, (cuuint64_t)pr.m, (cuuint64_t)pr.splits};
-        cuuint64_t strides[2] = {(cuuint64_t)(pr.ldo * 4), (cuuint64_t)(pr.part_stride * 4)};
-        cuuint32_t box[3] = {32u, 32u, 1u};
-        cuuint32_t est[3] = {1u, 1u, 1u};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pr.out, dims, strides, box, est,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        cuuint64_t dims[2] = {(cuuint64_t)pr.n_valid, (cuuint64_t)pr.m};
-        cuuint64_t strides[1] = {(cuuint64_t)(pr.ldo * es)};
-        cuuint32_t box[2] = {bf ? 64u : 32u, 32u};
-        cuuint32_t est[2] = {1u, 1u};
-        r = enc(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pr.out, dims,
-                strides, box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    if (r != CUDA_SUCCESS) return fail(LSN_ECUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+// The epilogue stores 16-byte pieces of output rows: the output (or partial slab) and its
+// row stride must keep every piece 16-byte aligned.
+static int check_out(const Problem& pr) {
+    if (pr.epi == EPI_F32_T) return LSN_OK;   // written element by element
+    const int64_t es = pr.epi == EPI_BF16 ? 2 : 4;
+    if ((pr.ldo * es) % 16 || pr.ldo < pr.n_valid || (reinterpret_cast<uintptr_t>(pr.out) & 15))
+        return fail(LSN_EINVAL, "gemm: output rows must be 16-byte aligned multiples of 16 bytes");
     return LSN_OK;
 }
 
-int choose_splits(int64_t units, int ksteps) {
-    const int64_t kTarget = 222;   // three waves of the 74 CTA pairs of a 148-SM part
-    if (units >= kTarget || ksteps < 4) return 1;
-    int64_t s = (kTarget + units - 1) / units;
-    if (s > ksteps / 2) s = ksteps / 2;
-    if (s > 32) s = 32;
-    return s < 1 ? 1 : (int)s;
+// ------------------------------------------------------------------ split-K planner
+
+namespace {
+
+constexpr int kPlanPairs = 74;                  // CTA pairs of a 148-SM part
+constexpr double kPlanEpiSteps = 7.0;           // epilogue of one tile, in k-step times
+constexpr double kPlanReduceBytesPerStep = 3.75e6;   // partial bytes reduced per k-step time
+constexpr double kPlanReduceLaunchSteps = 8.0;  // the reduction launch itself
+
+struct PlanProblem {
+    int64_t units;      // tiles of one split (M-pairs x N tiles)
+    int kb;             // k-steps the splits divide (a LoRA tail is left out of the estimate, so
+                        // that a problem gets the same splits with and without its tail)
+    double part_bytes;  // fp32 partial bytes of one split slab
+    double out_bytes;   // bytes of the final output
+};
+
+// Estimated launch time (in k-step times) of the static schedule with split counts s[].
+double plan_estimate(const PlanProblem* pp, int n, const int* s) {
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) total += pp[i].units * s[i];
+    const int P = total < kPlanPairs ? (int)total : kPlanPairs;
+    if (P < 1) return 0.0;
+    double load[kPlanPairs] = {0.0};
+    int64_t t = 0;
+    double reduce = 0.0;
+    bool any_split = false;
+    for (int i = 0; i < n; ++i) {
+        const int si = s[i];
+        for (int j = 0; j < si; ++j) {
+            // the tiles of split j: units consecutive schedule slots of equal length
+            const double len = (double)((int64_t)pp[i].kb * (j + 1) / si - (int64_t)pp[i].kb * j / si) +
+                               kPlanEpiSteps;
+            const int64_t c = pp[i].units;
+            const int64_t full = c / P, rem = c % P;
+            const int start = (int)(t % P);
+            for (int q = 0; q < P; ++q) {
+                const int64_t pos = (q - start + P) % P;   // order of pair q from the block start
+                load[q] += len * (double)(full + (pos < rem ? 1 : 0));
+            }
+            t += c;
+        }
+        if (si > 1) {
+            any_split = true;
+            reduce += (si * pp[i].part_bytes + pp[i].out_bytes) / kPlanReduceBytesPerStep;
+        }
+    }
+    double mk = 0.0;
+    for (int q = 0; q < P; ++q) mk = load[q] > mk ? load[q] : mk;
+    return mk + (any_split ? reduce + kPlanReduceLaunchSteps : 0.0);
+}
+
+std::mutex g_plan_mu;
+std::map<std::vector<int64_t>, std::vector<int>> g_plan_cache;
+
+}  // namespace
+
+void GemmPlan::resolve_splits() {
+    if (resolved_) return;
+    resolved_ = true;
+    const int n = p_.n_probs;
+    PlanProblem pp[kMaxProbs];
+    int s[kMaxProbs], maxs[kMaxProbs];
+    bool any_auto = false;
+    std::vector<int64_t> key;
+    key.reserve(8 * n);
+    for (int i = 0; i < n; ++i) {
+        const Problem& pr = p_.probs[i];
+        const int64_t tm = ((pr.m + kBM - 1) / kBM + 1) / 2, tn = (pr.n + pr.bn - 1) / pr.bn;
+        pp[i].units = tm * tn;
+        pp[i].kb = pr.ksteps_split;
+        pp[i].part_bytes = 4.0 * pr.m * pr.n;
+        pp[i].out_bytes = (double)pr.m * pr.n_valid * (pr.epi == EPI_BF16 ? 2 : 4);
+        maxs[i] = pr.ksteps_split / 2 < 32 ? pr.ksteps_split / 2 : 32;
+        if (maxs[i] < 1) maxs[i] = 1;
+        if (pr.splits == kAutoSplits) {
+            any_auto = true;
+            s[i] = 1;
+        } else {
+            s[i] = pr.splits < pr.ksteps_split ? pr.splits : (pr.ksteps_split > 0 ? pr.ksteps_split : 1);
+            maxs[i] = s[i];
+        }
+        key.insert(key.end(), {(int64_t)pr.m, (int64_t)pr.n, (int64_t)pr.bn, (int64_t)pr.ksteps_split,
+                               (int64_t)pr.epi, (int64_t)pr.n_valid, (int64_t)pr.splits});
+    }
+    if (any_auto) {
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lk(g_plan_mu);
+            auto it = g_plan_cache.find(key);
+            if (it != g_plan_cache.end()) {
+                for (int i = 0; i < n; ++i) s[i] = it->second[i];
+                hit = true;
+            }
+        }
+        if (!hit) {
+            // coordinate descent over the auto problems, two rounds, smallest split on ties
+            double best = plan_estimate(pp, n, s);
+            for (int round = 0; round < 2; ++round) {
+                for (int i = 0; i < n; ++i) {
+                    if (p_.probs[i].splits != kAutoSplits || pp[i].units >= 2 * kPlanPairs) continue;
+                    const int keep = s[i];
+                    int arg = keep;
+                    for (int c = 1; c <= maxs[i]; ++c) {
+                        s[i] = c;
+                        const double e = plan_estimate(pp, n, s);
+                        if (e < best - 1e-9 || (e <= best + 1e-9 && c < arg)) {
+                            best = e < best ? e : best;
+                            arg = c;
+                        }
+                    }
+                    s[i] = arg;
+                    best = plan_estimate(pp, n, s);
+                }
+            }
+            std::lock_guard<std::mutex> lk(g_plan_mu);
+            g_plan_cache[key] = std::vector<int>(s, s + n);
+        }
+    }
+    for (int i = 0; i < n; ++i) p_.probs[i].splits = s[i];
+}
+
+int GemmPlan::splits_of(int i) {
+    if (i < 0 || i >= p_.n_probs) return 0;
+    resolve_splits();
+    return p_.probs[i].splits;
 }
 
 GemmPlan::GemmPlan(bool dry) : dry_(dry) { memset(&p_, 0, sizeof(p_)); }
@@ -1015,7 +1107,7 @@ int GemmPlan::problem(int m, int n, int bn, int a_major, int epi, void* out, int
     if (p_.n_probs >= kMaxProbs) return status_ = fail(LSN_EINVAL, "gemm: too many problems");
     if (bn < kMinBN) bn = kMinBN;   // a pair MMA needs at least one 64-wide atom per CTA
     if (m < 1 || n < 1 || !(bn == 128 || bn == 256) || (!out && !dry_) || n_valid < 1 ||
-        n_valid > n || n_valid % 8 || splits < 1 || (reinterpret_cast<uintptr_t>(out) & 15))
+        n_valid > n || n_valid % 8 || splits < 0 || (reinterpret_cast<uintptr_t>(out) & 15))
         return status_ = fail(LSN_EINVAL, "gemm: bad problem");
     Problem& pr = p_.probs[p_.n_probs];
     memset(&pr, 0, sizeof(pr));
@@ -1088,12 +1180,13 @@ int GemmPlan::seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, i
     return s;
 }
 
-size_t GemmPlan::partial_bytes() const {
+size_t GemmPlan::partial_bytes() {
+    if (status_) return 0;
+    resolve_splits();
     size_t b = 0;
     for (int i = 0; i < p_.n_probs; ++i) {
         const Problem& pr = p_.probs[i];
-        const int splits = pr.splits > pr.ksteps_split ? pr.ksteps_split : pr.splits;
-        if (splits > 1) b += (size_t)splits * pr.m * pr.n * sizeof(float);
+        if (pr.splits > 1) b += (size_t)pr.splits * pr.m * pr.n * sizeof(float);
     }
     return b;
 }
@@ -1102,6 +1195,7 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     if (status_) return status_;
     if (p_.n_probs == 0) return LSN_OK;
     if (dry_) return LSN_OK;
+    resolve_splits();
     // partial-sum slabs for split problems
     struct Final { int epi; void* out; int64_t ldo; float alpha; const uint16_t* res; int64_t ldr; };
     Final fin[kMaxProbs];
@@ -1110,7 +1204,6 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     for (int i = 0; i < p_.n_probs; ++i) {
         Problem& pr = p_.probs[i];
         if (pr.seg_count == 0) return status_ = fail(LSN_EINVAL, "gemm: problem without segments");
-        if (pr.splits > pr.ksteps_split) pr.splits = pr.ksteps_split > 0 ? pr.ksteps_split : 1;
         pr.tiles_m = ((pr.m + kBM - 1) / kBM + 1) / 2;   // M-pairs: one per CTA pair
         pr.tiles_n = (pr.n + pr.bn - 1) / pr.bn;
         // raster group: as many M-pairs as keep their A rows (512 x K bf16 each) within
@@ -1139,7 +1232,7 @@ int GemmPlan::launch(cudaStream_t s, float* partial_ws, size_t ws_bytes) {
     }
     p_.total_tiles = tiles;
     for (int i = 0; i < p_.n_probs; ++i) {
-        int rc = encode_out_map(p_.probs[i], &p_.out_maps[i]);
+        int rc = check_out(p_.probs[i]);
         if (rc) return status_ = rc;
     }
     memcpy(p_.levels, nf4_levels(), sizeof(p_.levels));

@@ -8,6 +8,8 @@
 // is loaded and scaled by the producer warps (the LoRA B factor times s).  Accumulation is
 // fp32 in TMEM; the epilogue writes bf16, fp32, fp32 added into the output, fp32 transposed,
 // or fp32 split-K partials that one reduction launch per GEMM launch sums in a fixed order.
+// Split-K counts are chosen per launch by a planner that replays the kernel's static schedule
+// on a fixed 148-SM machine (GemmPlan::resolve_splits).
 #pragma once
 
 #include <cuda.h>
@@ -28,6 +30,8 @@ constexpr int kMaxMaps = 16;
 constexpr int kMaxNf4 = 8;
 constexpr int kMaxSegs = 20;
 constexpr int kMaxProbs = 16;
+// splits argument of GemmPlan::problem: let the launch planner choose the split-K count
+constexpr int kAutoSplits = 0;
 
 enum ASrc : int { A_KMAJOR = 0, A_MNMAJOR = 1 };
 enum BSrc : int {
@@ -92,7 +96,6 @@ struct Nf4Dev {
 
 struct GemmParams {   // 128-byte aligned through CUtensorMap
     CUtensorMap maps[kMaxMaps];
-    CUtensorMap out_maps[kMaxProbs];   // per problem: the output for the bulk-store epilogue
     Nf4Dev nf4[kMaxNf4];
     KSeg segs[kMaxSegs];
     Problem probs[kMaxProbs];
@@ -112,9 +115,10 @@ class GemmPlan {
     // kmajor: box 64 (cols) x box_rows; otherwise box 64 x 64.  Returns the map index or < 0.
     int map(const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows);
     int nf4(const void* base, int64_t n_out, int64_t k_in);
-    // Starts a problem; segments added next belong to it.
+    // Starts a problem; segments added next belong to it.  splits = kAutoSplits leaves the
+    // split-K count to the launch planner (see resolve_splits).
     int problem(int m, int n, int bn, int a_major, int epi, void* out, int64_t ldo, float alpha,
-                int n_valid, int splits = 1, const uint16_t* residual = nullptr,
+                int n_valid, int splits = kAutoSplits, const uint16_t* residual = nullptr,
                 int64_t ldr = 0);
     // tail: a LoRA contraction appended to the base one.  Tail segments follow every
     // non-tail segment of their problem, and all their k-steps belong to the last split, so
@@ -123,8 +127,10 @@ class GemmPlan {
     // Always a tail segment.
     int seg_scaled(int a_map, int a_k0, const uint16_t* b_ptr, int b_ld, int b_rows, int k_len,
                    float b_scale);
-    // Bytes of split-K partial workspace the launch needs (after clamping splits).
-    size_t partial_bytes() const;
+    // Bytes of split-K partial workspace the launch needs (after the planner's choice).
+    size_t partial_bytes();
+    // Split-K count of problem i (after the planner's choice).
+    int splits_of(int i);
     // Launches the GEMM and the split reductions (a dry plan only validates).
     int launch(cudaStream_t s, float* partial_ws, size_t ws_bytes);
     int status() const { return status_; }
@@ -133,6 +139,14 @@ class GemmPlan {
     void set_error_word(uint32_t* w) { ext_err_ = w; }
 
    private:
+    // Chooses the split count of every kAutoSplits problem (once per plan).  The estimate
+    // replays the kernel's static schedule -- tile t on CTA pair t mod P, every split of a
+    // problem in order -- on a fixed P = 74 pairs (a 148-SM part, whatever the device), so
+    // the choice, and with it the summation order, never depends on the device; it adds the
+    // time the fixed-order reduction needs for the fp32 partial slabs.  Among equal
+    // estimates the smaller split count wins.  Choices are cached by problem shapes.
+    void resolve_splits();
+    bool resolved_ = false;
     GemmParams p_;
     int n_maps_ = 0, n_nf4_ = 0, n_segs_ = 0;
     int map_box_[kMaxMaps] = {0};   // box rows of each map (the kernel's byte counts rely on it)
@@ -150,10 +164,6 @@ inline int pair_tiles(int64_t m, int64_t n, int bn) {
     return (int)(((mt + 1) / 2) * ((n + bnn - 1) / bnn));
 }
 
-// Split count for a launch of `units` pair tiles and a problem of `ksteps` contraction steps,
-// chosen for a fixed 148-SM (74-pair) machine so that the summation order never depends on
-// the device.
-int choose_splits(int64_t units, int ksteps);
 
 struct Nf4Levels {
     float v[16];

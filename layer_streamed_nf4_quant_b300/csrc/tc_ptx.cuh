@@ -107,6 +107,54 @@ __device__ __forceinline__ bool mbar_wait_bounded_cta(uint32_t bar, uint32_t par
     return mbar_wait_bounded_scoped<false>(bar, parity, abort, err, site);
 }
 
+// Non-blocking probes of a phase (mbarrier.test_wait): CTA-scope and cluster-scope acquire.
+// A probe of a phase that has already completed returns at once, where try_wait costs a few
+// hundred cycles even then; the MMA issuer, whose stages are nearly always ready, polls
+// with these.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Polls the phase with test_wait; bounded like mbar_wait_bounded_scoped (the abort flag and
+// the time limit are looked at every 256 probes).
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_poll_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t* err, uint32_t site) {
+    auto test = [&]() { return kClusterScope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity); };
+    if (test()) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (test()) return true;
+        if ((it & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                if (err) atomicCAS(err, 0u, (1u << 24) | site);
+                return false;
+            }
+        }
+    }
+}
+
 // Busy-waits for a fixed time (bounded); used on the abort path to let copies and MMAs
 // that are already in flight land before shared memory and TMEM are released.
 __device__ __forceinline__ void settle_ns(uint64_t ns) {

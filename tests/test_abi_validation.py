@@ -106,3 +106,19 @@ def test_adapter_disabled_forward_validation():
     assert _fwd(v, A=ALIGNED, B=0) == lsn.LSN_EINVAL
     assert _fwd(v, A=0, B=0, T=0, X=MISALIGNED) == lsn.LSN_EINVAL   # still validated
     assert "aligned" in _msg()
+
+
+def test_split_planner_choices_are_consistent():
+    """The launch planner's split counts (host only): large problems are not split, deep
+    skinny ones are, the counts stay within 1..32, repeated queries agree, and the workspace
+    query covers the partial sums of both forward launches."""
+    big = lsn.lora_fwd_plan(16384, 14336, 4096, 64)
+    assert big["y_splits"] == 1 and big["y_partial_bytes"] == 0
+    deep = lsn.lora_fwd_plan(128, 1024, 16384, 8)
+    assert 1 < deep["y_splits"] <= 32 and 1 < deep["t_splits"] <= 32
+    assert deep["y_partial_bytes"] == deep["y_splits"] * 128 * 1024 * 4
+    assert lsn.lora_fwd_plan(128, 1024, 16384, 8) == deep
+    need = lsn.lib.lora_nf4_workspace_bytes(128, 1024, 16384, 8)
+    assert need >= deep["t_partial_bytes"] + deep["y_partial_bytes"]
+    with pytest.raises(lsn.LsnError):
+        lsn.lora_fwd_plan(128, 1024, 100, 8)

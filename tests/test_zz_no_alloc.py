@@ -37,9 +37,14 @@ def _inputs(M, N, K, r, seed):
             _bf16(random_bf16((N, r), seed + 3, std=0.01)), _bf16(random_bf16((M, N), seed + 4)))
 
 
-@pytest.mark.parametrize("M,N,K,r,residual", [(128, 1024, 512, 8, False), (300, 256, 192, 16, True)])
+# shapes whose forward the library splits over K (so the static scratch is really used) and
+# whose fp32 partial sums still fit in the 16 MiB buffer
+@pytest.mark.parametrize("M,N,K,r,residual", [(128, 1024, 16384, 8, False), (200, 2048, 8192, 8, True)])
 def test_static_scratch_matches_workspace_entry_point(M, N, K, r, residual):
     import layer_streamed_nf4_quant_b300 as lsn
+    plan = lsn.lora_fwd_plan(M, N, K, r)
+    assert plan["y_splits"] > 1 and plan["t_splits"] > 1
+    assert 0 < plan["y_partial_bytes"] <= 16 << 20 and plan["t_partial_bytes"] <= 16 << 20
     W, X, A, B, R = _inputs(M, N, K, r, seed=M + N)
     packed = torch.from_numpy(lsn.nf4_pack(W)).cuda()
     res = R if residual else None
@@ -56,7 +61,8 @@ def test_static_scratch_matches_workspace_entry_point(M, N, K, r, residual):
 
 def test_static_scratch_refuses_shapes_beyond_its_buffer():
     import layer_streamed_nf4_quant_b300 as lsn
-    M, N, K, r = 2048, 4096, 512, 8                # split-K partials: 2 x 2048 x 4096 x 4 B = 64 MiB
+    M, N, K, r = 300, 4096, 16384, 8
+    assert lsn.lora_fwd_plan(M, N, K, r)["y_partial_bytes"] > 16 << 20   # 4 splits x 300 x 4096 x 4 B
     W, X, A, B, _ = _inputs(M, N, K, r, seed=1)
     packed = torch.from_numpy(lsn.nf4_pack(W)).cuda()
     with pytest.raises(lsn.LsnError) as e:
