@@ -11,15 +11,20 @@
 // (s*T*B^T forward, dT*A backward), so one fp32 TMEM accumulator holds the full result.
 //
 // Clusters of two CTAs (one per SM) share each tile through cta_group::2 MMAs; persistent
-// over a static tile order.  CTA roles (512 threads):
+// over a static tile order.  CTA roles (512 threads; warp w runs on sub-partition w % 4):
 //   warp 0       TMA producer of A (and of dense B) tiles
 //   warp 1       TMEM allocator (both CTAs) and, in the even CTA, the single-thread UMMA issuer
-//   warp 2       in the odd CTA: relays "stage full" to the even CTA
-//   warps 4-7    epilogue: TMEM -> registers -> swizzled shared staging -> bulk tensor stores
-//   warps 8-15   B producer: NF4 decode / scaled LoRA-B rows into shared memory
+//   warp 9       in the odd CTA: relays "stage full" to the even CTA
+//   warps 4-7    epilogue: TMEM -> registers -> swizzled shared staging -> coalesced stores
+//   warps 2, 3, 8, 10, 11, 12, 14, 15
+//                B producer: NF4 decode / scaled LoRA-B rows into shared memory
+// The issuer's sub-partition (1) carries no producer warp: the decode's ALU stream would take
+// the issue slots the MMA instructions need (measured: two decode-like warps beside the
+// issuer cut the pair-MMA rate to 69 %, the same warps on the other sub-partitions cost
+// nothing).
 // Every tile has a fixed K order and a fixed owner; split-K partials are reduced in split
-// order by gemm_reduce; the accumulate mode adds through the bulk reduce, one addition per
-// output element per launch.  So every launch is bit-reproducible and independent of where
+// order by gemm_reduce; the accumulate mode adds the old output value once per element per
+// launch.  So every launch is bit-reproducible and independent of where
 // the weights live.
 #include <cuda_bf16.h>
 #include <string.h>
@@ -37,8 +42,24 @@ namespace lsn {
 static_assert(sizeof(GemmParams) <= 32764, "kernel parameters must fit the 32 KB limit");
 
 constexpr int kRasterGroup = 8;   // at most this many M-pairs per raster group
-constexpr int kDequantWarp0 = 8;
 constexpr int kDequantWarpsPerStep = 4;   // one of the two producer groups
+constexpr int kRelayWarp = 9;
+
+// Producer warps: group * 4 + slot of warp w, or -1.  Each group of four spans sub-partitions
+// 0, 2 and 3; none is on sub-partition 1, the MMA issuer's.
+__device__ __forceinline__ int producer_index(int w) {
+    switch (w) {
+        case 8: return 0;
+        case 2: return 1;
+        case 10: return 2;
+        case 3: return 3;
+        case 12: return 4;
+        case 14: return 5;
+        case 11: return 6;
+        case 15: return 7;
+        default: return -1;
+    }
+}
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiStageBytes = 32 * 128;   // one staging tile: 32 rows of 128 bytes
 constexpr size_t kGemmSmemBytes = 1024 + (size_t)kStages * (kStageABytes + kStageBBytes) +
@@ -612,7 +633,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             volatile int no_abort = 0;   // this wait does not end early on an abort
             if (!ptx::mbar_wait_bounded(drain_bar, 0, &no_abort, p.err, kSiteDrain)) *abort_flag = 1;
         }
-    } else if (warp == 2) {
+    } else if (warp == kRelayWarp) {
         // ------------------------------------------- relay of stage readiness (rank 1)
         if (lane == 0 && !leader) {
             const uint32_t remote_pfull0 = ptx::mapa(pfull_bar(0), 0);
@@ -679,12 +700,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             else ptx::mbar_arrive_remote(acc_empty_dst);
             acc_phase ^= 1u;
         }
-    } else if (warp >= kDequantWarp0) {
+    } else if (producer_index(warp) >= 0) {
         // --------------------------------------------------------------- B producer
         // Two groups of four warps take alternate k-steps of the sequence, so two k-steps
         // are being decoded at once; each thread owns one 128-byte row of this CTA's half of
         // the B tile.
-        const int dt = threadIdx.x - kDequantWarp0 * 32;   // 0 .. 255
+        const int dt = producer_index(warp) * 32 + lane;   // 0 .. 255
         const int grp = dt >> 7;
         const int gt = dt & 127;
         SeqPos s;
