@@ -17,9 +17,12 @@ with its own clocks.  The timed regions run without per-launch instrumentation; 
 kernel's own time comes from a separate pass of the same steps with CUDA events around every
 GEMM launch.
 
---gpus N without a launcher starts N local ranks through torch.distributed.run; under a
-launcher every rank runs an independent replica of the workload on its own GPU (weak
-scaling) and the timing is the maximum over ranks.
+--gpus N without a launcher starts N local ranks through torch.distributed.run.  Under a
+launcher the ranks train data parallel over tokens: each rank holds the workload's M tokens
+of an N x M batch (weak scaling), streams the layers from its own pinned store, takes its
+loss means over the N x M tokens, and exchanges each layer's dA/dB (NCCL all-gather, then a
+fixed-order sum on the device) while the next layer's backward runs.  The timing is the
+maximum over ranks.
 """
 from __future__ import annotations
 
@@ -231,8 +234,8 @@ def max_over_ranks(pg, value, device):
 
 
 def whole_job_rate(world, tokens_per_rank, ms_per_step):
-    """Tokens per second of the whole job: every rank runs its own replica of the workload
-    (weak scaling), timed by the slowest rank."""
+    """Tokens per second of the whole job: every rank processes its own tokens_per_rank of the
+    global batch (weak scaling), timed by the slowest rank."""
     return world * tokens_per_rank / (ms_per_step * 1e-3)
 
 
@@ -359,9 +362,11 @@ def h2d_probe(torch, dev, store, layer_bytes, n_layers, slots, copy):
 # -------------------------------------------------------------------------- measure
 
 def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_pass, recompute, x0_bits, pg,
-            e2e_steps, gemm_steps, local):
+            e2e_steps, gemm_steps, local, world=1):
     """Warm-up, the timed region (no instrumentation), the GEMM timing pass and the end-to-end
-    loop of one workload; returns the measured numbers."""
+    loop of one workload; returns the measured numbers.  With world > 1 every step is one
+    data-parallel step: this rank's M tokens of a world x M batch, each layer's gradients
+    exchanged and summed across the ranks while the next layer's backward runs."""
     from layer_streamed_nf4_quant_b300 import workload
     L = desc.n_layers
     grads = [torch.empty(desc.lora_elems, dtype=torch.float32, device=dev) for _ in range(L)]
@@ -372,13 +377,18 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     ws = torch.empty(desc.workspace_bytes(M, recompute, ref_pass), dtype=torch.uint8, device=dev)
     x_ref = torch.empty((M, desc.d_model), dtype=torch.bfloat16, device=dev) if ref_pass else None
     compute = torch.cuda.Stream(device=dev)
+    dp = lsn.DataParallel(pg, desc, grads, compute) if world > 1 else None
 
     def step():
         kw = dict(stream=compute, recompute=recompute, reference_pass=ref_pass, x_ref_out=x_ref)
+        if dp is not None:
+            kw.update(token_count=world * M, grads_ready=dp.hook)
         if resident is not None:
             lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, resident_store=resident, **kw)
         else:
             lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, pool=pool, **kw)
+        if dp is not None:
+            dp.finish()
 
     for _ in range(warmup):
         step()
@@ -430,7 +440,7 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     out = {"ms": ms, "launches": launches, "pstats": pstats, "prof": prof, "gemm_steps": gemm_steps,
            "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "clocks": clk.summary(), "x0_bytes": x0.numel() * 2,
            "loss": float(loss_host.item())}
-    del ws, grads, x_ref
+    del ws, grads, x_ref, dp
     torch.cuda.empty_cache()
     return out
 
@@ -488,7 +498,7 @@ def main(argv=None):
                     help="read the layers from a resident device store instead of streaming them")
     ap.add_argument("--recompute", action="store_true",
                     help="keep only x_l per layer and recompute each layer in the reverse sweep")
-    ap.add_argument("--chunks", type=int, default=2, choices=[1, 2],
+    ap.add_argument("--chunks", type=int, default=1, choices=[1, 2],
                     help="copies per layer image: 2 = [header, q..up] and [o, down] (sub-layer streaming), "
                          "1 = whole-layer copies")
     ap.add_argument("--show-ranks", action="store_true",
@@ -565,9 +575,10 @@ def main(argv=None):
 
     ref_pass = bool(wl.get("reference_pass"))
     e2e_steps = args.e2e_steps or max(3, args.steps // 2)
+    # data parallel over tokens: this rank's contiguous M rows of a world x M batch
+    x0_bits = synth.stack_input(world * M, desc.d_model)[rank * M:(rank + 1) * M]
     main_m = measure(torch, lsn, dev, desc, M, args.steps, args.warmup, pool, resident, lora, ref_pass,
-                     args.recompute, synth.stack_input(M, desc.d_model), pg, e2e_steps,
-                     max(2, min(args.steps, 5)), local)
+                     args.recompute, x0_bits, pg, e2e_steps, max(2, min(args.steps, 5)), local, world)
     main_m["steps"] = args.steps
 
     sec = None
@@ -614,7 +625,9 @@ def main(argv=None):
                    "copies_per_layer_image": args.chunks if resident is None else 0,
                    "streamed_bytes_per_step": streamed_bytes, "l2": "inputs larger than L2 "
                    f"({streamed_bytes / 1e9:.2f} GB of layer images streamed per step)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "single GPU" if world == 1 else
+                   f"dp{world}: {M} tokens per rank of a {world * M}-token batch, per-layer dA/dB all-gather "
+                   "(NCCL) + fixed-order rank sum overlapping the next layer's backward"},
         "roofline": roof,
         "step_roofline": step_roof,
         "h2d_link": link,

@@ -344,6 +344,14 @@ typedef struct {
     uint16_t* const* lora_out;
 } lsn_adamw_state;
 
+/* Host callback of layer_stack_step_ex: called on the calling thread right after the
+ * backward of `layer` (its dA and dB in grad, `elems` fp32 values) has been enqueued on
+ * `stream`, and before that layer's fused AdamW update (if any) is enqueued.  It may enqueue
+ * work on `stream` or record an event there and work on another stream; it must not wait
+ * for the device.  Data-parallel training uses it to start each layer's gradient exchange
+ * while the next layer's backward runs. */
+typedef void (*lsn_layer_hook)(void* user, int32_t layer, float* grad, size_t elems, void* stream);
+
 typedef struct {
     int32_t recompute;
     int32_t reference_pass;
@@ -357,6 +365,15 @@ typedef struct {
     /* nullable, device fp32 [n_layers][M][d_model]: slice l receives dloss/dx_l, the gradient
      * with respect to layer l's input, right after layer l's backward. */
     float* dx_layers_out;
+    /* Tokens the loss means are taken over (0: M).  A data-parallel rank that holds M of a
+     * global batch of token_count tokens passes the global count: its loss, dx and dA/dB are
+     * then its exact share, and the ranks' sums are the global ones. */
+    int64_t token_count;
+    /* nullable: called after every layer's backward (see lsn_layer_hook).  Not together with
+     * adamw (LSN_EINVAL): the update has to see the exchanged gradients, so a step with a hook
+     * leaves the update to lsn_adamw_step once the hook's work is done. */
+    lsn_layer_hook grads_ready;
+    void* hook_user;
 } lsn_step_opts;
 
 size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const lsn_step_opts* opts);
@@ -369,6 +386,13 @@ size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const
  * bf16 [n] receives bf16(p).  All pointers 16-byte aligned.  Elementwise, in fp32. */
 int lsn_adamw_step(const lsn_adamw_hparams* hp, float* p, uint16_t* p_bf16, const float* g, float* m,
                    float* v, size_t n, void* stream);
+
+/* Fixed-order sum over ranks (the reduction of data-parallel gradients): out[i] =
+ * ((in[0][i] + in[1][i]) + in[2][i]) + ... in fp32, rank order, for i < n, where in is the
+ * device array [n_ranks][n] the ranks' gradients were gathered into.  Every rank that sums the
+ * same gathered array gets the same bits, whatever order a collective would have added them
+ * in.  out may alias in[0].  Pointers 16-byte aligned; n_ranks >= 1. */
+int lsn_sum_ranks(const float* in, int n_ranks, size_t n, float* out, void* stream);
 
 /* layer_stack_step with options.  x_ref_out (nullable, device bf16 [M x d_model]) receives
  * the reference-pass output when opts->reference_pass is set. */

@@ -13,8 +13,8 @@ import ctypes as C
 import numpy as np
 
 from ._lib import (LSN_ECORRUPT, LSN_EINVAL, LSN_ENOMEM, LSN_ESTATE, LSN_ETIMEOUT, LSN_OK,  # noqa: F401
-                   LsnError, check, lib, lsn_adamw_hparams, lsn_adamw_state, lsn_pool_stats, lsn_profile,
-                   lsn_stack_desc, lsn_step_opts, nf4_view)
+                   LsnError, check, lib, lsn_adamw_hparams, lsn_adamw_state, lsn_layer_hook, lsn_pool_stats,
+                   lsn_profile, lsn_stack_desc, lsn_step_opts, nf4_view)
 
 PROJ = ("q", "k", "v", "gate", "up", "o", "down")   # canonical projection order
 
@@ -326,22 +326,89 @@ class AdamW:
         return lsn_adamw_state(self.hp, *self._arrays)
 
 
+def shard_range(tokens: int, world: int, rank: int):
+    """Rows [begin, end) of a global batch of `tokens` rows that data-parallel rank `rank` of
+    `world` holds: contiguous, the first tokens % world ranks one row longer."""
+    if world < 1 or not 0 <= rank < world or tokens < world:
+        raise ValueError("need 0 <= rank < world <= tokens")
+    base, extra = divmod(tokens, world)
+    begin = rank * base + min(rank, extra)
+    return begin, begin + base + (1 if rank < extra else 0)
+
+
+def sum_ranks(gathered, n_ranks: int, out, stream=None):
+    """out = gathered[0] + gathered[1] + ... in rank order (fp32), gathered = [n_ranks * n]."""
+    n = out.numel()
+    check(lib.lsn_sum_ranks(_p(gathered), n_ranks, n, _p(out), _stream(stream)))
+
+
+class DataParallel:
+    """Token-sharded data parallelism over a torch.distributed process group (NCCL).
+
+    Every rank runs layer_stack_step on its own shard of the global batch, streaming the layers
+    from its own pinned store, with token_count = the global token count so that its loss and
+    gradients are its exact share.  Right after each layer's backward (the step's per-layer
+    hook) the layer's gradient blob is all-gathered on a communication stream and summed in rank
+    order by lsn_sum_ranks: every rank ends with the same bits, and the exchange of layer l
+    overlaps the backward of layer l - 1.  finish() makes the compute stream wait for the last
+    exchange."""
+
+    def __init__(self, dist, desc: StackDesc, grad_blobs, compute_stream, group=None):
+        torch = _torch()
+        self.dist, self.group = dist, group
+        self.world = dist.get_world_size(group)
+        self.grads = grad_blobs
+        self.compute = compute_stream
+        self.comm = torch.cuda.Stream(device=compute_stream.device)
+        self.gathered = torch.empty(self.world * desc.lora_elems, dtype=torch.float32, device=compute_stream.device)
+        self.error = None
+        self.hook = lsn_layer_hook(self._on_layer)   # pass as grads_ready; kept alive with the object
+
+    def _on_layer(self, user, layer, grad_ptr, elems, stream_ptr):
+        torch = _torch()
+        g = self.grads[layer]
+        if g.data_ptr() != grad_ptr or g.numel() != elems:
+            # an exception cannot cross the C caller: finish() raises it
+            self.error = f"DataParallel: layer {layer}'s gradient blob is not the one it was given"
+            return
+        ready = torch.cuda.Event()
+        ready.record(self.compute if stream_ptr is None else
+                     torch.cuda.ExternalStream(stream_ptr, device=self.compute.device))
+        self.comm.wait_event(ready)
+        with torch.cuda.stream(self.comm):
+            self.dist.all_gather_into_tensor(self.gathered, g, group=self.group)
+        sum_ranks(self.gathered, self.world, g, stream=self.comm)
+
+    def finish(self):
+        """The compute stream waits for every exchange of the step."""
+        torch = _torch()
+        if self.error:
+            err, self.error = self.error, None
+            raise RuntimeError(err)
+        done = torch.cuda.Event()
+        done.record(self.comm)
+        self.compute.wait_event(done)
+
+
 def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
                      resident_store=None, x_out=None, dx0=None, stream=None, recompute: bool = False,
                      reference_pass: bool = False, x_ref_out=None, adamw: "AdamW | None" = None,
-                     x_layers_out=None, dx_layers_out=None):
+                     x_layers_out=None, dx_layers_out=None, token_count: int = 0, grads_ready=None):
     """One forward + loss + backward pass over the stack (streamed through `pool`, or resident).
 
     recompute: keep only x_l per layer and recompute the rest in the reverse sweep.
     reference_pass: also run the adapter-disabled forward on the same streamed slots and write
     it to x_ref_out.
     x_layers_out: bf16 [L, M, d_model] receives every layer's output x_{l+1}.
-    dx_layers_out: fp32 [L, M, d_model] receives the gradient w.r.t. every layer's input x_l."""
+    dx_layers_out: fp32 [L, M, d_model] receives the gradient w.r.t. every layer's input x_l.
+    token_count: the token count the loss means are taken over (0: M; a data-parallel shard
+    passes the global batch's).
+    grads_ready: a lsn_layer_hook (e.g. DataParallel's) called after each layer's backward."""
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
     if not (recompute or reference_pass or x_ref_out is not None or adamw is not None or
-            x_layers_out is not None or dx_layers_out is not None):
+            x_layers_out is not None or dx_layers_out is not None or token_count or grads_ready is not None):
         check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                    _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws),
                                    ws.numel(), _stream(stream)))
@@ -352,6 +419,9 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
         o.adamw = C.pointer(st)
     o.x_layers_out = None if x_layers_out is None else x_layers_out.data_ptr()
     o.dx_layers_out = None if dx_layers_out is None else dx_layers_out.data_ptr()
+    o.token_count = int(token_count)
+    if grads_ready is not None:
+        o.grads_ready = grads_ready
     check(lib.layer_stack_step_ex(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                   C.byref(o), _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(x_ref_out),
                                   _p(dx0), _p(ws), ws.numel(), _stream(stream)))

@@ -50,10 +50,15 @@ class lsn_adamw_state(C.Structure):
                 ("v", C.POINTER(C.c_void_p)), ("lora_out", C.POINTER(C.c_void_p))]
 
 
+# void (*)(void* user, int32_t layer, float* grad, size_t elems, void* stream)
+lsn_layer_hook = C.CFUNCTYPE(None, C.c_void_p, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p)
+
+
 class lsn_step_opts(C.Structure):
     _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6),
                 ("adamw", C.POINTER(lsn_adamw_state)), ("x_layers_out", C.c_void_p),
-                ("dx_layers_out", C.c_void_p)]
+                ("dx_layers_out", C.c_void_p), ("token_count", C.c_int64), ("grads_ready", lsn_layer_hook),
+                ("hook_user", C.c_void_p)]
 
 
 class lsn_profile(C.Structure):
@@ -106,6 +111,7 @@ SIGNATURES = {
                              P, SZ, P]),
     "lsn_stack_workspace_bytes_ex": (SZ, [C.POINTER(lsn_stack_desc), I64, C.POINTER(lsn_step_opts)]),
     "lsn_adamw_step": (I, [C.POINTER(lsn_adamw_hparams), P, P, P, P, P, SZ, P]),
+    "lsn_sum_ranks": (I, [P, I, SZ, P, P]),
     "layer_stack_step_ex": (I, [P, P, C.POINTER(lsn_stack_desc), C.POINTER(lsn_step_opts), P, I64, C.POINTER(P),
                                 C.POINTER(P), P, P, P, P, P, SZ, P]),
 }

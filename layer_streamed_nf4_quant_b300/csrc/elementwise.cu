@@ -369,14 +369,14 @@ int launch_kv_sumsq(const uint16_t* y, int64_t ldy, int ok, int ov, int dkv, int
     return LSN_OK;
 }
 
-int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv_coef, float* dx, uint16_t* dx_bf,
-                float* xpart, const float* kvpart, float* loss, cudaStream_t s) {
-    const double md = (double)M * (double)D;
+int launch_loss(const uint16_t* x, int M, double norm_tokens, int D, int dkv, int n_layers, float kv_coef, float* dx,
+                uint16_t* dx_bf, float* xpart, const float* kvpart, float* loss, cudaStream_t s) {
+    const double md = norm_tokens * (double)D;
     loss_seed_kernel<<<kLossBlocks, 256, 0, s>>>(x, M, D, (float)(1.0 / md), dx, dx_bf, xpart);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     loss_final_kernel<<<1, 32, 0, s>>>(xpart, kvpart, n_layers, kLossBlocks, 1.0 / md,
-                                       (double)kv_coef / ((double)M * (double)dkv), loss);
+                                       (double)kv_coef / (norm_tokens * (double)dkv), loss);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
@@ -386,6 +386,36 @@ int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, in
                     float kv_coef, cudaStream_t s) {
     const int64_t work = (int64_t)M * (D / 8 + 2 * dkv / 8 + F / 8);
     dy_build_kernel<<<grid_for(work, 256), 256, 0, s>>>(dqa, y, dy, M, D, dkv, F, kv_coef);
+    note_launch();
+    LSN_CUDA_TRY(cudaGetLastError());
+    return LSN_OK;
+}
+
+// out[i] = sum over ranks in rank order (fp32, left to right); four elements per thread.
+// (no __restrict__: out may alias in[0]; each thread reads its elements before writing them)
+__global__ void sum_ranks_kernel(const float* in, int n_ranks, int64_t n, float* out) {
+    const int64_t n4 = n / 4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 acc = reinterpret_cast<const float4*>(in)[i];
+        for (int r = 1; r < n_ranks; ++r) {
+            const float4 v = reinterpret_cast<const float4*>(in + (int64_t)r * n)[i];
+            acc.x = __fadd_rn(acc.x, v.x);
+            acc.y = __fadd_rn(acc.y, v.y);
+            acc.z = __fadd_rn(acc.z, v.z);
+            acc.w = __fadd_rn(acc.w, v.w);
+        }
+        reinterpret_cast<float4*>(out)[i] = acc;
+    }
+    for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float acc = in[i];
+        for (int r = 1; r < n_ranks; ++r) acc = __fadd_rn(acc, in[(int64_t)r * n + i]);
+        out[i] = acc;
+    }
+}
+
+int launch_sum_ranks(const float* in, int n_ranks, int64_t n, float* out, cudaStream_t s) {
+    if (n == 0) return LSN_OK;
+    sum_ranks_kernel<<<grid_for((n + 3) / 4, 256), 256, 0, s>>>(in, n_ranks, n, out);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;

@@ -34,6 +34,7 @@ inline size_t a256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct Dims {
     int L, D, dkv, F, r, M, Ncat;
+    double norm_M;   // tokens the loss means are taken over (M, or a data-parallel batch's count)
     float s, eps, coef;
     int np[kNumProj];   // n_out per projection
     int kp[kNumProj];   // k_in per projection
@@ -74,6 +75,7 @@ bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
     o->F = d->d_ff;
     o->r = d->rank;
     o->M = (int)M;
+    o->norm_M = (double)M;
     o->Ncat = o->D + 2 * o->dkv + 2 * o->F;
     o->s = d->lora_alpha / (float)d->rank;
     o->eps = d->rms_eps;
@@ -346,7 +348,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         RC(c.run(g));
     }
     if (!c.dry)
-        RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / ((double)M * d.dkv)), c.s));
+        RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / (d.norm_M * d.dkv)), c.s));
     RC(c.need_qkvgu());
     if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
     {   // dT_p = bf16(s dY_p B_p)
@@ -431,6 +433,14 @@ size_t lsn_stack_workspace_bytes_ex(const lsn_stack_desc* desc, int64_t M, const
     return layout(c.d, nullptr, nullptr, &b, partial_need(desc, M, o), o) + 256;
 }
 
+int lsn_sum_ranks(const float* in, int n_ranks, size_t n, float* out, void* stream) {
+    if (!in || !out || n_ranks < 1 || (reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return fail(LSN_EINVAL, "lsn_sum_ranks: NULL or misaligned buffer, or no rank");
+    if (out != in && out < in + (size_t)n_ranks * n && in < out + n)
+        return fail(LSN_EINVAL, "lsn_sum_ranks: out overlaps in other than as in[0]");
+    return launch_sum_ranks(in, n_ranks, (int64_t)n, out, static_cast<cudaStream_t>(stream));
+}
+
 size_t lsn_stack_workspace_bytes(const lsn_stack_desc* desc, int64_t M) {
     return lsn_stack_workspace_bytes_ex(desc, M, nullptr);
 }
@@ -444,6 +454,12 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
     c.o = opts_or_default(opts);
     if (!x0 || !lora || !grads || !loss_out || !ws || (!pool && !resident_store))
         return fail(LSN_EINVAL, "layer_stack_step: NULL argument");
+    if (c.o.token_count < 0 || (c.o.token_count > 0 && c.o.token_count < M))
+        return fail(LSN_EINVAL, "layer_stack_step: token_count must be 0 or at least M");
+    if (c.o.token_count > 0) c.d.norm_M = (double)c.o.token_count;
+    if (c.o.adamw && c.o.grads_ready)
+        return fail(LSN_EINVAL, "layer_stack_step: AdamW inside the step cannot follow a gradient hook "
+                                "(the hook's exchange must finish first; run lsn_adamw_step after it)");
     if ((reinterpret_cast<uintptr_t>(ws) & 255) || (reinterpret_cast<uintptr_t>(x0) & 15))
         return fail(LSN_EINVAL, "layer_stack_step: ws must be 256-byte and x0 16-byte aligned");
     for (int l = 0; l < c.d.L; ++l)
@@ -503,8 +519,8 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         for (int l = 0; l < L; ++l)
             LSN_CUDA_TRY(cudaMemcpyAsync(c.o.x_layers_out + (size_t)l * act, c.b.x[l + 1], act * 2,
                                          cudaMemcpyDeviceToDevice, c.s));
-    RC(launch_loss(c.b.x[L], c.d.M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart, loss_out,
-                   c.s));
+    RC(launch_loss(c.b.x[L], c.d.M, c.d.norm_M, c.d.D, c.d.dkv, L, c.d.coef, c.b.dx, c.b.dx_bf, c.b.xpart, c.b.kvpart,
+                   loss_out, c.s));
     // reverse sweep, re-streaming every layer (and recomputing its activations if asked); the
     // backward of a layer starts with o and down, so those are copied first -- unless the
     // layer is recomputed, which starts with q..up
@@ -517,6 +533,7 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
         RC(image(l, rev != 0, &img));
         if (c.o.recompute) RC(fwd_layer(c, l, img, lora[l], true));
         RC(bwd_layer(c, l, img, lora[l], grads[l]));
+        if (c.o.grads_ready) c.o.grads_ready(c.o.hook_user, l, grads[l], lsn_lora_elems(desc), stream);
         if (c.o.dx_layers_out)
             LSN_CUDA_TRY(cudaMemcpyAsync(c.o.dx_layers_out + (size_t)l * act, c.b.dx, act * 4,
                                          cudaMemcpyDeviceToDevice, c.s));

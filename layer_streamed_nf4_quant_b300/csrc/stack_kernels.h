@@ -23,9 +23,12 @@ int launch_rmsnorm_bwd(const uint16_t* x, const float* rstd, const float* dh, fl
 int launch_silu_mul(const uint16_t* y, int64_t ldy, int og, int ou, uint16_t* a, int M, int F, cudaStream_t s);
 // part[2b], part[2b+1] = block sums of k^2 and v^2 (kLossBlocks blocks).
 int launch_kv_sumsq(const uint16_t* y, int64_t ldy, int ok, int ov, int dkv, int M, float* part, cudaStream_t s);
-// dx = x/(M*D) (fp32 and bf16) and the scalar loss from x's and the layers' k/v sums.
-int launch_loss(const uint16_t* x, int M, int D, int dkv, int n_layers, float kv_coef, float* dx, uint16_t* dx_bf,
-                float* xpart, const float* kvpart, float* loss, cudaStream_t s);
+// dx = x/(T*D) (fp32 and bf16) and the scalar loss from x's and the layers' k/v sums, with
+// T = norm_tokens the token count the means are taken over (M, or a data-parallel batch's).
+int launch_loss(const uint16_t* x, int M, double norm_tokens, int D, int dkv, int n_layers, float kv_coef, float* dx,
+                uint16_t* dx_bf, float* xpart, const float* kvpart, float* loss, cudaStream_t s);
+// out = in[0] + in[1] + ... (rank order, fp32), in = [n_ranks][n].
+int launch_sum_ranks(const float* in, int n_ranks, int64_t n, float* out, cudaStream_t s);
 // dY_cat = [dq | 2c k/(M dkv) | 2c v/(M dkv) | dgate | dup] in bf16.
 int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
                     float kv_coef, cudaStream_t s);

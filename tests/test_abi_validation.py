@@ -122,3 +122,41 @@ def test_split_planner_choices_are_consistent():
     assert need >= deep["t_partial_bytes"] + deep["y_partial_bytes"]
     with pytest.raises(lsn.LsnError):
         lsn.lora_fwd_plan(128, 1024, 100, 8)
+
+
+def _step_ex(opts, M=64, L=2):
+    P = C.c_void_p
+    desc = lsn.StackDesc(n_layers=L, d_model=256, d_kv=256, d_ff=512, rank=8)
+    lora = (P * L)(*[ALIGNED] * L)
+    grads = (P * L)(*[ALIGNED] * L)
+    return lsn.lib.layer_stack_step_ex(None, P(ALIGNED), C.byref(desc.c), C.byref(opts), P(ALIGNED), M, lora, grads,
+                                       P(ALIGNED), None, None, None, P(0x100000), 1 << 40, None)
+
+
+def test_data_parallel_step_options_are_validated():
+    from layer_streamed_nf4_quant_b300._lib import lsn_step_opts, lsn_layer_hook, lsn_adamw_state
+    for tc in (-1, 63):                        # negative, or fewer tokens than this rank holds
+        o = lsn_step_opts(0, 0)
+        o.token_count = tc
+        assert _step_ex(o) == lsn.LSN_EINVAL
+        assert "token_count" in _msg()
+    hook = lsn_layer_hook(lambda *a: None)
+    st = lsn_adamw_state()
+    o = lsn_step_opts(0, 0)
+    o.grads_ready = hook
+    o.adamw = C.pointer(st)
+    assert _step_ex(o) == lsn.LSN_EINVAL
+    assert "hook" in _msg()
+
+
+def test_sum_ranks_arguments_are_validated():
+    P = C.c_void_p
+    s = lsn.lib.lsn_sum_ranks
+    assert s(None, 2, 64, P(ALIGNED), None) == lsn.LSN_EINVAL
+    assert s(P(ALIGNED), 2, 64, None, None) == lsn.LSN_EINVAL
+    assert s(P(ALIGNED), 0, 64, P(0x20000), None) == lsn.LSN_EINVAL
+    assert s(P(MISALIGNED), 2, 64, P(0x20000), None) == lsn.LSN_EINVAL
+    assert s(P(ALIGNED), 2, 64, P(MISALIGNED), None) == lsn.LSN_EINVAL
+    # out may be in[0] but no other part of the gathered array
+    assert s(P(ALIGNED), 2, 64, P(ALIGNED + 64 * 4), None) == lsn.LSN_EINVAL
+    assert "overlaps" in _msg()

@@ -1,4 +1,4 @@
-"""The N > 1 path of bench.py, on CPU: every rank runs its own replica of the workload, the
+"""The N > 1 path of bench.py, on CPU: every rank runs its own token shard of the batch, the
 ranks agree on the slowest rank's time, and the whole-job rate counts all ranks' tokens.
 Two gloo ranks in spawned processes (rendezvous on 127.0.0.1)."""
 import os
