@@ -391,31 +391,43 @@ int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, in
     return LSN_OK;
 }
 
-// out[i] = sum over ranks in rank order (fp32, left to right); four elements per thread.
+// out[i] = sum over ranks in rank order (fp32, left to right).
 // (no __restrict__: out may alias in[0]; each thread reads its elements before writing them)
+// kVec: four elements per thread through 16-byte accesses.  Rank r's row starts at in + r*n,
+// which is 16-byte aligned for every r only when n is a multiple of 4 (in and out are), so
+// the launcher takes the vector form only then.
+template <bool kVec>
 __global__ void sum_ranks_kernel(const float* in, int n_ranks, int64_t n, float* out) {
-    const int64_t n4 = n / 4;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-        float4 acc = reinterpret_cast<const float4*>(in)[i];
-        for (int r = 1; r < n_ranks; ++r) {
-            const float4 v = reinterpret_cast<const float4*>(in + (int64_t)r * n)[i];
-            acc.x = __fadd_rn(acc.x, v.x);
-            acc.y = __fadd_rn(acc.y, v.y);
-            acc.z = __fadd_rn(acc.z, v.z);
-            acc.w = __fadd_rn(acc.w, v.w);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (kVec) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = first; i < n4; i += stride) {
+            float4 acc = reinterpret_cast<const float4*>(in)[i];
+            for (int r = 1; r < n_ranks; ++r) {
+                const float4 v = reinterpret_cast<const float4*>(in + (int64_t)r * n)[i];
+                acc.x = __fadd_rn(acc.x, v.x);
+                acc.y = __fadd_rn(acc.y, v.y);
+                acc.z = __fadd_rn(acc.z, v.z);
+                acc.w = __fadd_rn(acc.w, v.w);
+            }
+            reinterpret_cast<float4*>(out)[i] = acc;
         }
-        reinterpret_cast<float4*>(out)[i] = acc;
-    }
-    for (int64_t i = n4 * 4 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        float acc = in[i];
-        for (int r = 1; r < n_ranks; ++r) acc = __fadd_rn(acc, in[(int64_t)r * n + i]);
-        out[i] = acc;
+    } else {
+        for (int64_t i = first; i < n; i += stride) {
+            float acc = in[i];
+            for (int r = 1; r < n_ranks; ++r) acc = __fadd_rn(acc, in[(int64_t)r * n + i]);
+            out[i] = acc;
+        }
     }
 }
 
 int launch_sum_ranks(const float* in, int n_ranks, int64_t n, float* out, cudaStream_t s) {
     if (n == 0) return LSN_OK;
-    sum_ranks_kernel<<<grid_for((n + 3) / 4, 256), 256, 0, s>>>(in, n_ranks, n, out);
+    if (n % 4 == 0)
+        sum_ranks_kernel<true><<<grid_for(n / 4, 256), 256, 0, s>>>(in, n_ranks, n, out);
+    else
+        sum_ranks_kernel<false><<<grid_for(n, 256), 256, 0, s>>>(in, n_ranks, n, out);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
