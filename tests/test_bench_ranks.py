@@ -61,8 +61,11 @@ def test_gpus_flag_starts_one_rank_per_gpu_without_a_launcher():
     import subprocess
     import sys
     env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
-    r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--show-ranks"], capture_output=True,
-                       text=True, timeout=180, env=env)
+    for attempt in range(2):   # the port bench.py picks can be taken before the launcher binds it
+        r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--show-ranks"], capture_output=True,
+                           text=True, timeout=180, env=env)
+        if r.returncode == 0:
+            break
     assert r.returncode == 0, r.stderr
     ranks = sorted((json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")), key=lambda d: d["rank"])
     assert [d["rank"] for d in ranks] == [0, 1]
