@@ -75,19 +75,17 @@ def gemm_source_hash():
 
 
 def measured_traffic(workload):
-    """DRAM bytes per GEMM launch from the committed ncu summary (profiles/tc_gemm_dram_traffic.md:
-    its `kernel_source_sha256` and `traffic_bytes_per_launch <workload> <bytes>` lines), or None
-    once the GEMM kernel's sources differ from the ones the counters were taken on."""
+    """DRAM bytes per GEMM launch from the committed ncu record (profiles/tc_gemm_traffic.json),
+    or None once the GEMM kernel's sources differ from the ones the counters were taken on."""
     try:
-        with open(os.path.join(ROOT, "profiles", "tc_gemm_dram_traffic.md")) as f:
-            lines = [l.split() for l in f.read().splitlines()]
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "tc_gemm_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    sha = [l[1] for l in lines if len(l) == 2 and l[0] == "kernel_source_sha256"]
-    if not sha or sha[-1] != gemm_source_hash():
+    if rec.get("kernel_source_sha256") != gemm_source_hash():
         return None
-    v = [l[2] for l in lines if len(l) == 3 and l[0] == "traffic_bytes_per_launch" and l[1] == workload]
-    return int(v[-1]) if v else None
+    v = rec.get("traffic_bytes_per_launch", {}).get(workload)
+    return int(v) if v is not None else None
 
 
 def analytic_step_flops(M, L=32, D=4096, dkv=1024, F=14336, r=64, reference_pass=False):
