@@ -338,18 +338,31 @@ struct EpiArgs {
     int64_t ldr;
 };
 
+// Register copies of kernel parameters.  The empty asm hides where the value came from, so the
+// compiler keeps it in a register (or spills it to the stack) instead of re-reading the
+// parameter inside the epilogue loop, where a constant-cache miss costs hundreds of cycles.
+__device__ __forceinline__ int reg_copy(int v) { asm volatile("mov.b32 %0, %0;" : "+r"(v)); return v; }
+__device__ __forceinline__ float reg_copy(float v) { asm volatile("mov.b32 %0, %0;" : "+f"(v)); return v; }
+__device__ __forceinline__ int64_t reg_copy(int64_t v) { asm volatile("mov.b64 %0, %0;" : "+l"(v)); return v; }
+template <class T>
+__device__ __forceinline__ T* reg_copy(T* v) {
+    uint64_t u = reinterpret_cast<uint64_t>(v);
+    asm volatile("mov.b64 %0, %0;" : "+l"(u));
+    return reinterpret_cast<T*>(u);
+}
+
 __device__ __forceinline__ EpiArgs epi_args(const Problem& pr, int split) {
     EpiArgs a;
-    a.epi = pr.epi;
-    a.m = pr.m;
-    a.n_valid = pr.n_valid;
-    a.split = split;
-    a.alpha = pr.alpha;
-    a.out = pr.out;
-    a.ldo = pr.ldo;
-    a.part_stride = pr.part_stride;
-    a.residual = pr.residual;
-    a.ldr = pr.ldr;
+    a.epi = reg_copy(pr.epi);
+    a.m = reg_copy(pr.m);
+    a.n_valid = reg_copy(pr.n_valid);
+    a.split = reg_copy(split);
+    a.alpha = reg_copy(pr.alpha);
+    a.out = reg_copy(pr.out);
+    a.ldo = reg_copy(pr.ldo);
+    a.part_stride = reg_copy(pr.part_stride);
+    a.residual = reg_copy(pr.residual);
+    a.ldr = reg_copy(pr.ldr);
     return a;
 }
 
@@ -673,25 +686,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tc_gemm_kernel(const __grid_c
             auto chunk_c = [&](int i) { return (i & ((1 << per_h_log) - 1)) * 32; };
             uint32_t ra[32], rb[32];
             __syncwarp();
+            const int bn = reg_copy(pr.bn), m0 = reg_copy(ti.m0), n0 = reg_copy(ti.n0);
             if (ea.epi == EPI_BF16) {
                 // chunk pairs (the N tile is 128 or 256 wide, so pairs never straddle a block)
                 for (int i = 0; i < n_chunks; i += 2) {
-                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i) * pr.bn + chunk_c(i)), ra);
-                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
+                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i) * bn + chunk_c(i)), ra);
+                    ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * bn + chunk_c(i + 1)), rb);
                     ptx::tmem_ld_wait(ra);
                     ptx::tmem_ld_wait(rb);
-                    epi_pair_bf16(ea, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, rb, est, lane, pol_out);
+                    epi_pair_bf16(ea, m0 + chunk_h(i) * 128 + q * 32, n0 + chunk_c(i), ra, rb, est, lane, pol_out);
                 }
             } else {
-            ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * pr.bn + chunk_c(0)), ra);
+            ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(0) * bn + chunk_c(0)), ra);
             ptx::tmem_ld_wait(ra);
             for (int i = 0; i < n_chunks; i += 2) {
-                if (i + 1 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * pr.bn + chunk_c(i + 1)), rb);
-                epi_chunk(ea, ti.m0 + chunk_h(i) * 128 + q * 32, ti.n0 + chunk_c(i), ra, est, lane, pol_out);
+                if (i + 1 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 1) * bn + chunk_c(i + 1)), rb);
+                epi_chunk(ea, m0 + chunk_h(i) * 128 + q * 32, n0 + chunk_c(i), ra, est, lane, pol_out);
                 if (i + 1 >= n_chunks) break;
                 ptx::tmem_ld_wait(rb);
-                if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * pr.bn + chunk_c(i + 2)), ra);
-                epi_chunk(ea, ti.m0 + chunk_h(i + 1) * 128 + q * 32, ti.n0 + chunk_c(i + 1), rb, est, lane, pol_out);
+                if (i + 2 < n_chunks) ptx::tmem_ld32_issue(tq + (uint32_t)(chunk_h(i + 2) * bn + chunk_c(i + 2)), ra);
+                epi_chunk(ea, m0 + chunk_h(i + 1) * 128 + q * 32, n0 + chunk_c(i + 1), rb, est, lane, pol_out);
                 if (i + 2 < n_chunks) ptx::tmem_ld_wait(ra);
             }
             }
