@@ -154,24 +154,46 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ y, int64_t ldy, int
 
 // ------------------------------------------------------------------ loss and seeds
 
-// Per-block sums of k^2 and v^2 over rows blockIdx.x, blockIdx.x + kLossBlocks, ...
+// Per-block sums of k^2 and v^2 over rows blockIdx.x, blockIdx.x + kLossBlocks, ...  The
+// block's rows are cut into 16-byte pieces (dkv / 8 per row, for k and for v) and thread t
+// takes pieces t, t + 256, ... in order, four at a time so that their loads are in flight
+// together; every thread's order and the block tree are fixed, so the sums do not depend on
+// timing.
 __global__ void kv_sumsq_kernel(const uint16_t* __restrict__ y, int64_t ldy, int ok, int ov, int dkv,
                                 int M, float* __restrict__ part) {
     __shared__ float sh[256];
     float sk = 0.f, sv = 0.f;
-    for (int row = blockIdx.x; row < M; row += gridDim.x) {
-        for (int c = threadIdx.x * 8; c < dkv; c += 256 * 8) {
-            const uint4 k = *reinterpret_cast<const uint4*>(y + (int64_t)row * ldy + ok + c);
-            const uint4 v = *reinterpret_cast<const uint4*>(y + (int64_t)row * ldy + ov + c);
-            const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
+    const int ppr = dkv / 8;   // pieces per row
+    const int rows = blockIdx.x < M ? (M - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int64_t total = (int64_t)rows * ppr;
+    auto piece = [&](int64_t p, uint4& k, uint4& v) {
+        const int64_t row = blockIdx.x + (p / ppr) * (int64_t)gridDim.x;
+        const int c = (int)(p % ppr) * 8;
+        k = *reinterpret_cast<const uint4*>(y + row * ldy + ok + c);
+        v = *reinterpret_cast<const uint4*>(y + row * ldy + ov + c);
+    };
+    auto add = [&](const uint4& k, const uint4& v) {
+        const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sk = __fadd_rn(sk, __fmul_rn(bf_lo(kw[j]), bf_lo(kw[j])));
-                sk = __fadd_rn(sk, __fmul_rn(bf_hi(kw[j]), bf_hi(kw[j])));
-                sv = __fadd_rn(sv, __fmul_rn(bf_lo(vw[j]), bf_lo(vw[j])));
-                sv = __fadd_rn(sv, __fmul_rn(bf_hi(vw[j]), bf_hi(vw[j])));
-            }
+        for (int j = 0; j < 4; ++j) {
+            sk = __fadd_rn(sk, __fmul_rn(bf_lo(kw[j]), bf_lo(kw[j])));
+            sk = __fadd_rn(sk, __fmul_rn(bf_hi(kw[j]), bf_hi(kw[j])));
+            sv = __fadd_rn(sv, __fmul_rn(bf_lo(vw[j]), bf_lo(vw[j])));
+            sv = __fadd_rn(sv, __fmul_rn(bf_hi(vw[j]), bf_hi(vw[j])));
         }
+    };
+    int64_t p = threadIdx.x;
+    for (; p + 3 * 256 < total; p += 4 * 256) {
+        uint4 k[4], v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) piece(p + u * 256, k[u], v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) add(k[u], v[u]);
+    }
+    for (; p < total; p += 256) {
+        uint4 k, v;
+        piece(p, k, v);
+        add(k, v);
     }
     const float tk = block_sum256(sk, sh);
     __syncthreads();
@@ -211,20 +233,37 @@ __global__ void loss_seed_kernel(const uint16_t* __restrict__ x, int M, int D, f
 }
 
 // loss = 0.5 * Sx / (M D) + sum_l coef (Sk_l + Sv_l) / (M dkv), summed in a fixed order in fp64.
+// Sum over the kLossFinalThreads threads of one block, in a fixed tree order (fp64).
+constexpr int kLossFinalThreads = 128;
+__device__ __forceinline__ double block_sum_f64(double v, double* sh) {
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int s = kLossFinalThreads / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+        __syncthreads();
+    }
+    const double t = sh[0];
+    __syncthreads();   // sh is reused by the next sum
+    return t;
+}
+
+// loss = 0.5 * sum(x^2) / (M D) + coef / (M dkv) * sum over layers of sum(k^2 + v^2), from the
+// per-block partial sums.  One block; thread t takes the blocks b = t, t + 128, ... in order and
+// the threads' sums meet in a fixed tree, so the result does not depend on timing.
 __global__ void loss_final_kernel(const float* __restrict__ xpart, const float* __restrict__ kvpart,
                                   int n_layers, int nb, double inv_md, double coef_inv_mkv,
                                   float* __restrict__ loss) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    __shared__ double sh[kLossFinalThreads];
     double sx = 0.0;
-    for (int b = 0; b < nb; ++b) sx += (double)xpart[b];
-    double l = 0.5 * sx * inv_md;
+    for (int b = threadIdx.x; b < nb; b += kLossFinalThreads) sx += (double)xpart[b];
+    double l = 0.5 * block_sum_f64(sx, sh) * inv_md;
     for (int layer = 0; layer < n_layers; ++layer) {
+        const float* kv = kvpart + (size_t)layer * nb * 2;
         double skv = 0.0;
-        for (int b = 0; b < nb; ++b)
-            skv += (double)kvpart[(size_t)layer * nb * 2 + 2 * b] + (double)kvpart[(size_t)layer * nb * 2 + 2 * b + 1];
-        l += coef_inv_mkv * skv;
+        for (int b = threadIdx.x; b < nb; b += kLossFinalThreads) skv += (double)kv[2 * b] + (double)kv[2 * b + 1];
+        l += coef_inv_mkv * block_sum_f64(skv, sh);
     }
-    *loss = (float)l;
+    if (threadIdx.x == 0) *loss = (float)l;
 }
 
 // ------------------------------------------------------------- backward dY assembly
@@ -375,7 +414,7 @@ int launch_loss(const uint16_t* x, int M, double norm_tokens, int D, int dkv, in
     loss_seed_kernel<<<kLossBlocks, 256, 0, s>>>(x, M, D, (float)(1.0 / md), dx, dx_bf, xpart);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
-    loss_final_kernel<<<1, 32, 0, s>>>(xpart, kvpart, n_layers, kLossBlocks, 1.0 / md,
+    loss_final_kernel<<<1, kLossFinalThreads, 0, s>>>(xpart, kvpart, n_layers, kLossBlocks, 1.0 / md,
                                        (double)kv_coef / (norm_tokens * (double)dkv), loss);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());

@@ -8,7 +8,7 @@
 
 namespace lsn {
 
-constexpr int kLossBlocks = 128;   // fixed grid of the loss reductions (fixes their order)
+constexpr int kLossBlocks = 296;   // fixed grid of the loss reductions (fixes their order): 2 per SM
 
 // h = bf16(x * rstd), rstd = (mean(x^2) + eps)^-1/2.  If header is non-null, block 0 also
 // checks the layer image tag against `layer` and records a mismatch in the error word.
