@@ -128,6 +128,79 @@ __global__ void rmsnorm_bwd_kernel(const uint16_t* __restrict__ x, const float* 
     }
 }
 
+// The same backward with one 128-thread block per row, for D <= 4096: each thread keeps its
+// (at most four) 16-byte pieces of x and dh in registers between the dot product and the
+// update, so the row is read once.  The dot product adds each thread's pieces in order, then
+// the warps' sums in warp order: a fixed order.
+constexpr int kNormBwdThreads = 128;
+constexpr int kNormBwdPieces = 4;   // 16-byte pieces of x per thread: D <= 8 * 128 * 4
+__global__ void __launch_bounds__(kNormBwdThreads) rmsnorm_bwd_row_kernel(const uint16_t* __restrict__ x,
+                                                                         const float* __restrict__ rstd,
+                                                                         const float* __restrict__ dh,
+                                                                         float* __restrict__ dx,
+                                                                         uint16_t* __restrict__ dx_bf, int D) {
+    __shared__ float wsum[kNormBwdThreads / 32];
+    const int row = blockIdx.x;
+    const int np = D / 8;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)row * D);
+    const float4* dr = reinterpret_cast<const float4*>(dh + (int64_t)row * D);
+    uint4 xv[kNormBwdPieces];
+    float4 d0[kNormBwdPieces], d1[kNormBwdPieces];
+#pragma unroll
+    for (int i = 0; i < kNormBwdPieces; ++i) {
+        const int c = threadIdx.x + i * kNormBwdThreads;
+        if (c < np) {
+            xv[i] = xr[c];
+            d0[i] = dr[2 * c];
+            d1[i] = dr[2 * c + 1];
+        }
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNormBwdPieces; ++i) {
+        const int c = threadIdx.x + i * kNormBwdThreads;
+        if (c < np) {
+            const uint4 v = xv[i];
+            dot = __fadd_rn(dot, __fmul_rn(d0[i].x, bf_lo(v.x)));
+            dot = __fadd_rn(dot, __fmul_rn(d0[i].y, bf_hi(v.x)));
+            dot = __fadd_rn(dot, __fmul_rn(d0[i].z, bf_lo(v.y)));
+            dot = __fadd_rn(dot, __fmul_rn(d0[i].w, bf_hi(v.y)));
+            dot = __fadd_rn(dot, __fmul_rn(d1[i].x, bf_lo(v.z)));
+            dot = __fadd_rn(dot, __fmul_rn(d1[i].y, bf_hi(v.z)));
+            dot = __fadd_rn(dot, __fmul_rn(d1[i].z, bf_lo(v.w)));
+            dot = __fadd_rn(dot, __fmul_rn(d1[i].w, bf_hi(v.w)));
+        }
+    }
+    dot = warp_sum_bcast(dot);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = dot;
+    __syncthreads();
+    float tot = wsum[0];
+#pragma unroll
+    for (int w = 1; w < kNormBwdThreads / 32; ++w) tot = __fadd_rn(tot, wsum[w]);
+    const float r = rstd[row];
+    const float c3 = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), __fdiv_rn(tot, (float)D));
+    float4* xo = reinterpret_cast<float4*>(dx + (int64_t)row * D);
+    uint4* bo = reinterpret_cast<uint4*>(dx_bf + (int64_t)row * D);
+#pragma unroll
+    for (int i = 0; i < kNormBwdPieces; ++i) {
+        const int c = threadIdx.x + i * kNormBwdThreads;
+        if (c < np) {
+            const uint4 v = xv[i];
+            const float4 g0 = xo[2 * c], g1 = xo[2 * c + 1];
+            const float xs[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
+                                 bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
+            const float ds[8] = {d0[i].x, d0[i].y, d0[i].z, d0[i].w, d1[i].x, d1[i].y, d1[i].z, d1[i].w};
+            float gs[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                gs[j] = __fsub_rn(__fadd_rn(gs[j], __fmul_rn(r, ds[j])), __fmul_rn(c3, xs[j]));
+            xo[2 * c] = make_float4(gs[0], gs[1], gs[2], gs[3]);
+            xo[2 * c + 1] = make_float4(gs[4], gs[5], gs[6], gs[7]);
+            bo[c] = make_uint4(bf2(gs[0], gs[1]), bf2(gs[2], gs[3]), bf2(gs[4], gs[5]), bf2(gs[6], gs[7]));
+        }
+    }
+}
+
 // --------------------------------------------------------------------------- SiLU-mul
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
@@ -388,7 +461,10 @@ int launch_tag_check(const void* header, uint32_t layer, cudaStream_t s) {
 
 int launch_rmsnorm_bwd(const uint16_t* x, const float* rstd, const float* dh, float* dx, uint16_t* dx_bf,
                        int M, int D, cudaStream_t s) {
-    rmsnorm_bwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, rstd, dh, dx, dx_bf, M, D);
+    if (D <= 8 * kNormBwdThreads * kNormBwdPieces)
+        rmsnorm_bwd_row_kernel<<<M, kNormBwdThreads, 0, s>>>(x, rstd, dh, dx, dx_bf, D);
+    else
+        rmsnorm_bwd_kernel<<<(M + 7) / 8, 256, 0, s>>>(x, rstd, dh, dx, dx_bf, M, D);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;
