@@ -1,12 +1,15 @@
-"""GPU parity at the full token count of the 8 x 2048-token workload (M = 16384), checked
-where the oracle cannot run the whole problem:
+"""GPU parity at the full token count of the 8 x 2048-token workload (M = 16384), one layer:
 
 * sampled rows: the layer stack is row-independent apart from the normalisation of its
   means, so x_1 and dx0 on 256 sampled rows are compared with the oracle run on those rows
   alone (the oracle divides its means by the full M);
-* additivity over rows: every loss term is a mean over rows, so the gradients of the full
-  run equal the sum of the gradients of 64 runs over disjoint 256-row slices, each scaled
-  by 256 / M, and the loss equals the mean of the slice losses.
+* the LoRA gradients of all 16384 rows against the oracle: the oracle runs the rows in
+  eight 2048-row chunks, each with its means taken over the full M, and adds the chunks'
+  dA, dB in fp64 -- by linearity of the gradient in the per-row loss terms that sum is the
+  full batch's gradient (about two minutes of fp64 CPU work);
+* additivity over rows on the GPU: the gradients of the full run equal the sum of the
+  gradients of 64 runs over disjoint 256-row slices, each scaled by 256 / M, and the loss
+  equals the mean of the slice losses.
 
 The launch configuration (tiles, splits, raster) is the one the 16384-token bench uses.
 """
@@ -45,6 +48,37 @@ def test_sampled_rows_match_oracle(full):
     assert np.max(np.abs(x - ref["x_last"])) / np.max(np.abs(ref["x_last"])) <= FWD_TOL
     dx0 = out["dx0"].double().cpu().numpy()[rows]
     assert np.linalg.norm(dx0 - ref["dx0"]) / np.linalg.norm(ref["dx0"]) <= GRAD_TOL
+
+
+def test_full_batch_gradients_match_oracle(full):
+    import synth
+    from oracle import nf4 as onf4
+    from oracle import stack as ostack
+    from oracle.nf4 import bf16_value
+    st, out = full
+    d = st.desc
+    W = synth.layer_weights(0, d.d_model, d.d_kv, d.d_ff)
+    A, B = synth.layer_lora(0, d.rank, d.d_model, d.d_kv, d.d_ff)
+    layers = [({p: onf4.dequantize(onf4.quantize(W[p])) for p in W},
+               {p: bf16_value(A[p]).astype(np.float64) for p in A},
+               {p: bf16_value(B[p]).astype(np.float64) for p in B})]
+    del W
+    x0 = bf16_value(st.x0_bits).astype(np.float64)
+    chunk = 2048
+    dA = dB = None
+    for c0 in range(0, M_FULL, chunk):
+        ref = ostack.stack_forward_backward(x0[c0:c0 + chunk], layers, d.scale, token_count=M_FULL)
+        if dA is None:
+            dA, dB = ref["dA"][0], ref["dB"][0]
+        else:
+            dA = {p: dA[p] + ref["dA"][0][p] for p in dA}
+            dB = {p: dB[p] + ref["dB"][0][p] for p in dB}
+        del ref
+    gA, gB = _grad_views(st, out["grads"][0])
+    for p in gA:
+        for got, want in ((gA[p], dA[p]), (gB[p], dB[p])):
+            assert np.all(np.isfinite(got))
+            assert np.linalg.norm(got - want) / np.linalg.norm(want) <= GRAD_TOL, p
 
 
 def test_gradients_add_up_over_row_slices(full):
