@@ -362,7 +362,7 @@ def h2d_probe(torch, dev, store, layer_bytes, n_layers, slots, copy):
 # -------------------------------------------------------------------------- measure
 
 def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_pass, recompute, x0_bits, pg,
-            e2e_steps, gemm_steps, local, world=1):
+            e2e_steps, gemm_steps, local, world=1, bwd_weights=0):
     """Warm-up, the timed region (no instrumentation), the GEMM timing pass and the end-to-end
     loop of one workload; returns the measured numbers.  With world > 1 every step is one
     data-parallel step: this rank's M tokens of a world x M batch, each layer's gradients
@@ -374,13 +374,14 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     x0_host = x0.cpu().pin_memory()
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
-    ws = torch.empty(desc.workspace_bytes(M, recompute, ref_pass), dtype=torch.uint8, device=dev)
+    ws = torch.empty(desc.workspace_bytes(M, recompute, ref_pass, bwd_weights), dtype=torch.uint8, device=dev)
     x_ref = torch.empty((M, desc.d_model), dtype=torch.bfloat16, device=dev) if ref_pass else None
     compute = torch.cuda.Stream(device=dev)
     dp = lsn.DataParallel(pg, desc, grads, compute) if world > 1 else None
 
     def step():
-        kw = dict(stream=compute, recompute=recompute, reference_pass=ref_pass, x_ref_out=x_ref)
+        kw = dict(stream=compute, recompute=recompute, reference_pass=ref_pass, x_ref_out=x_ref,
+                  bwd_weights=bwd_weights)
         if dp is not None:
             kw.update(token_count=world * M, grads_ready=dp.hook)
         if resident is not None:
@@ -501,6 +502,8 @@ def main(argv=None):
     ap.add_argument("--chunks", type=int, default=1, choices=[1, 2],
                     help="copies per layer image: 2 = [header, q..up] and [o, down] (sub-layer streaming), "
                          "1 = whole-layer copies")
+    ap.add_argument("--bwd-weights", type=int, default=0, choices=[0, 1, 2],
+                    help="backward GEMMs' W: 0 automatic, 1 NF4 decoded in the GEMM, 2 decoded to bf16 first")
     ap.add_argument("--show-ranks", action="store_true",
                     help="print each rank's world size, rank and device binding as JSON and exit")
     args = ap.parse_args(argv)
@@ -578,7 +581,8 @@ def main(argv=None):
     # data parallel over tokens: this rank's contiguous M rows of a world x M batch
     x0_bits = synth.stack_input(world * M, desc.d_model)[rank * M:(rank + 1) * M]
     main_m = measure(torch, lsn, dev, desc, M, args.steps, args.warmup, pool, resident, lora, ref_pass,
-                     args.recompute, x0_bits, pg, e2e_steps, max(2, min(args.steps, 5)), local, world)
+                     args.recompute, x0_bits, pg, e2e_steps, max(2, min(args.steps, 5)), local, world,
+                     args.bwd_weights)
     main_m["steps"] = args.steps
 
     sec = None
@@ -620,6 +624,7 @@ def main(argv=None):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl["name"], "tokens_per_step": M, "layers": L, "lora_rank": desc.rank,
                    "recompute": bool(args.recompute), "reference_pass": ref_pass,
+                   "bwd_weights": args.bwd_weights,
                    "bytes_streamed_per_step_vs_plain_step":
                        (ps["bytes_copied"] / args.steps) / (2 * L * desc.image_bytes) if ps else 0.0,
                    "copies_per_layer_image": args.chunks if resident is None else 0,

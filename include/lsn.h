@@ -355,7 +355,14 @@ typedef void (*lsn_layer_hook)(void* user, int32_t layer, float* grad, size_t el
 typedef struct {
     int32_t recompute;
     int32_t reference_pass;
-    int32_t reserved[6];
+    /* How the backward's two transposed GEMMs ([dq | da] and dh) read W:
+     *   1: packed NF4, decoded by the GEMM's producer warps into its operand tiles;
+     *   2: each layer's W decoded once into bf16 scratch in the workspace (the same values,
+     *      bit for bit, so the results are identical), then read by TMA as a dense operand;
+     *   0: 2 from 8192 tokens up, else 1.
+     * Other values: LSN_EINVAL.  The workspace size depends on it (lsn_stack_workspace_bytes_ex). */
+    int32_t bwd_weights;
+    int32_t reserved[5];
     /* nullable: when set, each layer's AdamW update runs in the reverse sweep right after
      * that layer's dA/dB are written (they are still written to grads). */
     const lsn_adamw_state* adamw;

@@ -275,10 +275,12 @@ class StackDesc:
         return {"q": (D, D), "k": (dkv, D), "v": (dkv, D), "gate": (F, D), "up": (F, D), "o": (D, D),
                 "down": (D, F)}[p]
 
-    def workspace_bytes(self, M: int, recompute: bool = False, reference_pass: bool = False) -> int:
-        if not (recompute or reference_pass):
+    def workspace_bytes(self, M: int, recompute: bool = False, reference_pass: bool = False,
+                        bwd_weights: int = 0) -> int:
+        if not (recompute or reference_pass or bwd_weights):
             return int(lib.lsn_stack_workspace_bytes(C.byref(self.c), M))
         o = lsn_step_opts(1 if recompute else 0, 1 if reference_pass else 0)
+        o.bwd_weights = int(bwd_weights)
         return int(lib.lsn_stack_workspace_bytes_ex(C.byref(self.c), M, C.byref(o)))
 
     def pack_layer(self, layer: int, W: dict, dst: np.ndarray | None = None, n_threads: int = 0) -> np.ndarray:
@@ -393,7 +395,8 @@ class DataParallel:
 def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, pool: StreamPool | None = None,
                      resident_store=None, x_out=None, dx0=None, stream=None, recompute: bool = False,
                      reference_pass: bool = False, x_ref_out=None, adamw: "AdamW | None" = None,
-                     x_layers_out=None, dx_layers_out=None, token_count: int = 0, grads_ready=None):
+                     x_layers_out=None, dx_layers_out=None, token_count: int = 0, grads_ready=None,
+                     bwd_weights: int = 0):
     """One forward + loss + backward pass over the stack (streamed through `pool`, or resident).
 
     recompute: keep only x_l per layer and recompute the rest in the reverse sweep.
@@ -403,12 +406,15 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
     dx_layers_out: fp32 [L, M, d_model] receives the gradient w.r.t. every layer's input x_l.
     token_count: the token count the loss means are taken over (0: M; a data-parallel shard
     passes the global batch's).
-    grads_ready: a lsn_layer_hook (e.g. DataParallel's) called after each layer's backward."""
+    grads_ready: a lsn_layer_hook (e.g. DataParallel's) called after each layer's backward.
+    bwd_weights: 0 automatic, 1 NF4 decoded inside the backward GEMMs, 2 each layer's weights
+    decoded to bf16 scratch first (identical results; size ws with the same value)."""
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])
     if not (recompute or reference_pass or x_ref_out is not None or adamw is not None or
-            x_layers_out is not None or dx_layers_out is not None or token_count or grads_ready is not None):
+            x_layers_out is not None or dx_layers_out is not None or token_count or grads_ready is not None or
+            bwd_weights):
         check(lib.layer_stack_step(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),
                                    _p(x0), x0.shape[0], lo, gr, _p(loss_out), _p(x_out), _p(dx0), _p(ws),
                                    ws.numel(), _stream(stream)))
@@ -420,6 +426,7 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
     o.x_layers_out = None if x_layers_out is None else x_layers_out.data_ptr()
     o.dx_layers_out = None if dx_layers_out is None else dx_layers_out.data_ptr()
     o.token_count = int(token_count)
+    o.bwd_weights = int(bwd_weights)
     if grads_ready is not None:
         o.grads_ready = grads_ready
     check(lib.layer_stack_step_ex(pool.handle if pool is not None else None, _p(resident_store), C.byref(desc.c),

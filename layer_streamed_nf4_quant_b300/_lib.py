@@ -55,7 +55,7 @@ lsn_layer_hook = C.CFUNCTYPE(None, C.c_void_p, C.c_int32, C.c_void_p, C.c_size_t
 
 
 class lsn_step_opts(C.Structure):
-    _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("reserved", C.c_int32 * 6),
+    _fields_ = [("recompute", C.c_int32), ("reference_pass", C.c_int32), ("bwd_weights", C.c_int32), ("reserved", C.c_int32 * 5),
                 ("adamw", C.POINTER(lsn_adamw_state)), ("x_layers_out", C.c_void_p),
                 ("dx_layers_out", C.c_void_p), ("token_count", C.c_int64), ("grads_ready", lsn_layer_hook),
                 ("hook_user", C.c_void_p)]

@@ -338,7 +338,7 @@ extern "C" {
 
 const char* lsn_last_error(void) { return g_err; }
 
-int lsn_abi_version(void) { return 3; }
+int lsn_abi_version(void) { return 4; }
 
 uint64_t lsn_launch_count(void) { return g_launches.load(); }
 

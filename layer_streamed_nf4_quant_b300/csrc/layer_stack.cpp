@@ -56,6 +56,8 @@ struct Buffers {
     float* xpart = nullptr;
     float* partial = nullptr;
     size_t partial_bytes = 0;
+    // backward with decoded weights: one layer's W_o, W_down, then W_q..W_up, as bf16
+    uint16_t* wdec = nullptr;
     // reference (adapter disabled) pass: residual stream ping-pong and per-layer scratch
     uint16_t* xr[2] = {nullptr, nullptr};
     uint16_t* hr = nullptr;
@@ -92,6 +94,22 @@ bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
     o->coff[3] = o->D + 2 * o->dkv;
     o->coff[4] = o->D + 2 * o->dkv + o->F;
     return true;
+}
+
+// Tokens from which the backward decodes each layer's weights to bf16 once and runs its two
+// transposed GEMMs on them (bwd_weights = 0): the decode costs about 0.1 ms per layer, and the
+// dense operand makes those GEMMs about 10 % faster, which pays from a few thousand tokens.
+constexpr int kDenseBwdTokens = 8192;
+
+bool dense_bwd(const Dims& d, const lsn_step_opts& o) {
+    return o.bwd_weights == 2 || (o.bwd_weights == 0 && d.M >= kDenseBwdTokens);
+}
+
+// bf16 elements of the decoded-weight scratch: the larger of [W_o, W_down] and [W_q .. W_up].
+size_t wdec_elems(const Dims& d) {
+    size_t od = (size_t)d.np[kO] * d.kp[kO] + (size_t)d.np[kDown] * d.kp[kDown], qu = 0;
+    for (int p = 0; p < 5; ++p) qu += (size_t)d.np[p] * d.kp[p];
+    return od > qu ? od : qu;
 }
 
 // Lays the activations and scratch out in ws (base == nullptr: only sizes).  Returns bytes.
@@ -149,6 +167,7 @@ size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size
         b->yr = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
         b->ar = reinterpret_cast<uint16_t*>(take(M * d.F * 2));
     }
+    if (dense_bwd(d, o)) b->wdec = reinterpret_cast<uint16_t*>(take(wdec_elems(d) * 2));
     b->partial = reinterpret_cast<float*>(take(partial_bytes));
     b->partial_bytes = partial_bytes;
     return off;
@@ -187,6 +206,25 @@ struct Ctx {
         return g.launch(s, b.partial, b.partial_bytes);
     }
     const void* mat(const uint8_t* img, int p) const { return img ? img + img_off[p] : nullptr; }
+    // decoded-weight scratch: bf16 matrix p of a group laid out from `first` on
+    uint16_t* wd(int first, int p) const {
+        if (!b.wdec) return nullptr;
+        size_t off = 0;
+        for (int q = first; q < p; ++q) off += (size_t)d.np[q] * d.kp[q];
+        return b.wdec + off;
+    }
+    // decodes projections first .. last of the layer image into the scratch
+    int decode(const uint8_t* img, int first, int last) {
+        if (dry) return LSN_OK;
+        Nf4Dev w[kNumProj];
+        uint16_t* out[kNumProj];
+        for (int p = first; p <= last; ++p) {
+            const int rc = nf4_view_dev(mat(img, p), d.np[p], d.kp[p], &w[p - first]);
+            if (rc) return rc;
+            out[p - first] = wd(first, p);
+        }
+        return nf4_dequant_many(w, out, last - first + 1, s);
+    }
     const uint16_t* A(const uint16_t* lo, int p) const { return lo ? lo + la[p] : nullptr; }
     const uint16_t* B(const uint16_t* lo, int p) const { return lo ? lo + lb[p] : nullptr; }
     float* dA(float* g, int p) const { return g ? g + la[p] : nullptr; }
@@ -317,6 +355,8 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         g.seg(mdx, 0, B_TMA_MN, mbd, 0, 0, D);
         RC(c.run(g));
     }
+    const bool dense = dense_bwd(c.d, c.o);
+    if (dense) RC(c.decode(img, kO, kDown));
     {   // dB_o, dB_d, dA_o, dA_d and [dq | da] = dx' [W_o | W_d] + dT_od [A_o ; A_d]
         GemmPlan g(c.dry);
         int mdx_mn = g.map(b.dx_bf, M, D, D, 64);
@@ -328,8 +368,10 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         int mdtod = g.map(b.dtod, M, 2 * r, 2 * r, kBM);
         int mao = g.map(c.A(lora, kO), r, D, D, 64);
         int mad = g.map(c.A(lora, kDown), r, F, F, 64);
-        int vo = g.nf4(c.mat(img, kO), D, D);
-        int vd = g.nf4(c.mat(img, kDown), D, F);
+        // W_o, W_down: packed NF4 decoded by the GEMM, or the bf16 copies decoded above
+        const int bsrc = dense ? B_TMA_MN : B_NF4_MN;
+        const int vo = dense ? g.map(c.wd(kO, kO), D, D, D, 64) : g.nf4(c.mat(img, kO), D, D);
+        const int vd = dense ? g.map(c.wd(kO, kDown), D, F, F, 64) : g.nf4(c.mat(img, kDown), D, F);
         const int ws = kAutoSplits, xs = kAutoSplits;
         g.problem(D, r, 64, A_MNMAJOR, EPI_F32, c.dB(grad, kO), r, d.s, r, ws);
         g.seg(mdx_mn, 0, B_TMA_MN, mtod_mn, 0, 0, M);
@@ -340,10 +382,10 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         g.problem(F, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, kDown), F, 1.0f, r, ws);
         g.seg(ma_mn, 0, B_TMA_MN, mdtod_mn, 0, r, M);
         g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dqa, D + F, 1.0f, D, xs);
-        g.seg(mdx, 0, B_NF4_MN, vo, 0, 0, D);
+        g.seg(mdx, 0, bsrc, vo, 0, 0, D);
         g.seg(mdtod, 0, B_TMA_MN, mao, 0, 0, r, true);
         g.problem(M, F, 256, A_KMAJOR, EPI_F32, b.dqa ? b.dqa + D : nullptr, D + F, 1.0f, F, xs);
-        g.seg(mdx, 0, B_NF4_MN, vd, 0, 0, D);
+        g.seg(mdx, 0, bsrc, vd, 0, 0, D);
         g.seg(mdtod, r, B_TMA_MN, mad, 0, 0, r, true);
         RC(c.run(g));
     }
@@ -351,6 +393,7 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / (d.norm_M * d.dkv)), c.s));
     RC(c.need_qkvgu());
     if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
+    if (dense) RC(c.decode(img, kQ, kUp));
     {   // dT_p = bf16(s dY_p B_p)
         GemmPlan g(c.dry);
         int mdy = g.map(b.dy, M, d.Ncat, d.Ncat, kBM);
@@ -382,8 +425,8 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         }
         g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dh, D, 1.0f, D, kAutoSplits);
         for (int p = 0; p < 5; ++p) {
-            int v = g.nf4(c.mat(img, p), d.np[p], D);
-            g.seg(mdy, d.coff[p], B_NF4_MN, v, 0, 0, d.np[p]);
+            const int v = dense ? g.map(c.wd(kQ, p), d.np[p], D, D, 64) : g.nf4(c.mat(img, p), d.np[p], D);
+            g.seg(mdy, d.coff[p], dense ? B_TMA_MN : B_NF4_MN, v, 0, 0, d.np[p]);
         }
         g.seg(mdtcat, 0, B_TMA_MN, macat, 0, 0, 5 * r, true);
         RC(c.run(g));
@@ -457,6 +500,8 @@ int layer_stack_step_ex(lsn_pool* pool, const void* resident_store, const lsn_st
     if (c.o.token_count < 0 || (c.o.token_count > 0 && c.o.token_count < M))
         return fail(LSN_EINVAL, "layer_stack_step: token_count must be 0 or at least M");
     if (c.o.token_count > 0) c.d.norm_M = (double)c.o.token_count;
+    if (c.o.bwd_weights < 0 || c.o.bwd_weights > 2)
+        return fail(LSN_EINVAL, "layer_stack_step: bwd_weights must be 0, 1 or 2");
     if (c.o.adamw && c.o.grads_ready)
         return fail(LSN_EINVAL, "layer_stack_step: AdamW inside the step cannot follow a gradient hook "
                                 "(the hook's exchange must finish first; run lsn_adamw_step after it)");

@@ -168,15 +168,10 @@ int nf4_dequant(const nf4_view* W, uint16_t* out, void* stream) {
     Nf4Layout L;
     if (!nf4_layout(W->n_out, W->k_in, &L) || !al16(W->base) || !al16(out))
         return fail(LSN_EINVAL, "nf4_dequant: bad view or alignment");
-    const uint8_t* b = static_cast<const uint8_t*>(W->base);
     Nf4Dev d;
-    d.codes = b + L.codes;
-    d.absmax = b + L.absmax;
-    d.scale = reinterpret_cast<const float*>(b + L.scale);
-    d.offset = reinterpret_cast<const float*>(b + L.offset);
-    d.n_out = W->n_out;
-    d.k_in = W->k_in;
-    return nf4_dequant_launch(d, out, static_cast<cudaStream_t>(stream));
+    const int rc = nf4_view_dev(W->base, W->n_out, W->k_in, &d);
+    if (rc) return rc;
+    return nf4_dequant_many(&d, &out, 1, static_cast<cudaStream_t>(stream));
 }
 
 int lora_nf4_fwd(const nf4_view* W, const uint16_t* X, int64_t M, const uint16_t* A, const uint16_t* B,

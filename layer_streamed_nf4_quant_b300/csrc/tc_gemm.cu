@@ -6,8 +6,9 @@
 // matters so much"): the frozen NF4 base W is applied forward (y = x W^T) and transposed
 // backward (dX = dY W) once per layer while the layer sits in a streamed VRAM slot.  Here W
 // is decoded 64 weights (one absmax block) at a time by producer warps directly into the
-// 128-byte-swizzled shared-memory operand tiles that tcgen05.mma reads; bf16 W never exists
-// in HBM.  The LoRA branch enters as extra contraction steps of the same accumulator
+// 128-byte-swizzled shared-memory operand tiles that tcgen05.mma reads, so bf16 W need not
+// exist in HBM (nf4_dequant_many writes it there when a caller prefers a dense operand: the
+// backward at large token counts).  The LoRA branch enters as extra contraction steps of the same accumulator
 // (s*T*B^T forward, dT*A backward), so one fp32 TMEM accumulator holds the full result.
 //
 // Clusters of two CTAs (one per SM) share each tile through cta_group::2 MMAs; persistent
@@ -866,21 +867,53 @@ __global__ void gemm_reduce_kernel(const __grid_constant__ ReduceJobs jobs) {
     }
 }
 
-// --------------------------------------------------------------------- dequant (tests)
+// --------------------------------------------------------------------------- dequant
 
-__global__ void nf4_dequant_kernel(Nf4Dev w, Nf4Levels lvl, uint16_t* __restrict__ out) {
-    const int64_t nb = w.n_out * (w.k_in / 64);
-    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nb;
-         b += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = b / (w.k_in / 64);
-        const int64_t col0 = (b - row * (w.k_in / 64)) * 64;
-        Nf4Block bk;
-        nf4_load_block(w, row, col0, bk);
-        uint32_t o[32];
-        nf4_decode_regs(bk, lvl.v, o);
-        uint4* dst = reinterpret_cast<uint4*>(out + row * w.k_in + col0);
+// Many matrices at once, 32 blocks per warp; the decoded rows are transposed through shared
+// memory so that every store instruction writes 512 contiguous bytes.
+struct DequantParams {
+    Nf4Dev w[kMaxNf4];
+    uint16_t* out[kMaxNf4];
+    int64_t group_begin[kMaxNf4 + 1];   // first 32-block group of each matrix; [n] = total
+    int n;
+    Nf4Levels lvl;
+};
+constexpr int kDequantWarps = 8;
+
+__global__ void __launch_bounds__(kDequantWarps * 32) nf4_dequant_many_kernel(const __grid_constant__ DequantParams p) {
+    __shared__ __align__(128) uint8_t stage[kDequantWarps][32 * 128];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t base = ptx::smem_u32(&stage[warp][0]);
+    const int64_t total = p.group_begin[p.n];
+    for (int64_t g = (int64_t)blockIdx.x * kDequantWarps + warp; g < total;
+         g += (int64_t)gridDim.x * kDequantWarps) {
+        int m = 0;
+        while (m + 1 < p.n && g >= p.group_begin[m + 1]) ++m;
+        const Nf4Dev& w = p.w[m];
+        const int64_t nb = w.n_out * (w.k_in >> 6);
+        const int64_t b0 = (g - p.group_begin[m]) * 32;
+        const int64_t b = b0 + lane;
+        if (b < nb) {
+            const int64_t kb = w.k_in >> 6;
+            const int64_t row = b / kb;
+            Nf4Block bk;
+            nf4_load_block(w, row, (b - row * kb) * 64, bk);
+            uint32_t o[32];
+            nf4_decode_regs(bk, p.lvl.v, o);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            for (int c = 0; c < 8; ++c)
+                st_shared_v4(base + (uint32_t)lane * 128u + (((uint32_t)c ^ (uint32_t)(lane & 7)) << 4), o[4 * c],
+                             o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        }
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(p.out[m] + b0 * 64);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int idx = j * 32 + lane;   // 16-byte piece of the group's 4 KB
+            const int r = idx >> 3, c = idx & 7;
+            if (b0 + r < nb) dst[idx] = ld_shared_v4(base + (uint32_t)r * 128u + (((uint32_t)c ^ (uint32_t)(r & 7)) << 4));
+        }
+        __syncwarp();
     }
 }
 
@@ -1339,14 +1372,40 @@ static int launch_reduce(const ReduceJobs& jobs, cudaStream_t s) {
     return LSN_OK;
 }
 
-int nf4_dequant_launch(const Nf4Dev& w, uint16_t* out, cudaStream_t s) {
-    Nf4Levels l;
-    memcpy(l.v, nf4_levels(), sizeof(l.v));
-    const int64_t nb = w.n_out * (w.k_in / 64);
-    int64_t blocks = (nb + 255) / 256;
-    const int64_t cap = (int64_t)num_sms() * 16;
+int nf4_view_dev(const void* base, int64_t n_out, int64_t k_in, Nf4Dev* out) {
+    Nf4Layout L;
+    if (!base || !out || (reinterpret_cast<uintptr_t>(base) & 15) || !nf4_layout(n_out, k_in, &L))
+        return fail(LSN_EINVAL, "nf4: bad NF4 view");
+    const uint8_t* b = static_cast<const uint8_t*>(base);
+    out->codes = b + L.codes;
+    out->absmax = b + L.absmax;
+    out->scale = reinterpret_cast<const float*>(b + L.scale);
+    out->offset = reinterpret_cast<const float*>(b + L.offset);
+    out->n_out = n_out;
+    out->k_in = k_in;
+    return LSN_OK;
+}
+
+int nf4_dequant_many(const Nf4Dev* w, uint16_t* const* out, int n, cudaStream_t s) {
+    if (n < 1 || n > kMaxNf4 || !w || !out) return fail(LSN_EINVAL, "nf4_dequant_many: bad matrix count");
+    DequantParams p;
+    memset(&p, 0, sizeof(p));
+    p.n = n;
+    memcpy(p.lvl.v, nf4_levels(), sizeof(p.lvl.v));
+    int64_t g = 0;
+    for (int i = 0; i < n; ++i) {
+        if (!out[i] || (reinterpret_cast<uintptr_t>(out[i]) & 15) || w[i].n_out < 1 || w[i].k_in < 64 || w[i].k_in % 64)
+            return fail(LSN_EINVAL, "nf4_dequant_many: bad output or shape");
+        p.w[i] = w[i];
+        p.out[i] = out[i];
+        p.group_begin[i] = g;
+        g += (w[i].n_out * (w[i].k_in / 64) + 31) / 32;
+    }
+    p.group_begin[n] = g;
+    int64_t blocks = (g + kDequantWarps - 1) / kDequantWarps;
+    const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    nf4_dequant_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, l, out);
+    nf4_dequant_many_kernel<<<(unsigned)blocks, kDequantWarps * 32, 0, s>>>(p);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;

@@ -168,7 +168,12 @@ inline int pair_tiles(int64_t m, int64_t n, int bn) {
 struct Nf4Levels {
     float v[16];
 };
-// Test-only decode of a whole packed matrix to bf16 in HBM (same decode as the GEMM).
-int nf4_dequant_launch(const Nf4Dev& w, uint16_t* out, cudaStream_t s);
+// Device view of a packed NF4 matrix at base (16-byte aligned).
+int nf4_view_dev(const void* base, int64_t n_out, int64_t k_in, Nf4Dev* out);
+// Decodes n (<= kMaxNf4) packed NF4 matrices into dense row-major bf16 [n_out x k_in] at
+// out[i] (16-byte aligned), in one launch: the same values, bit for bit, that the GEMM's
+// producer warps write into its operand tiles.  Each warp decodes 32 consecutive blocks
+// (4 KB of output) and stores them through shared memory in whole 512-byte rows.
+int nf4_dequant_many(const Nf4Dev* w, uint16_t* const* out, int n, cudaStream_t s);
 
 }  // namespace lsn

@@ -28,7 +28,7 @@ def test_exports_every_declared_symbol():
     for n in names:
         assert hasattr(lsn.lib, n), n
         assert n in _lib.SIGNATURES, f"binding lacks {n}"
-    assert lsn.lib.lsn_abi_version() == 3
+    assert lsn.lib.lsn_abi_version() == 4
 
 
 def test_codebook_matches_oracle_bitwise():

@@ -149,6 +149,21 @@ def test_data_parallel_step_options_are_validated():
     assert "hook" in _msg()
 
 
+def test_backward_weight_mode_is_validated_and_sized():
+    from layer_streamed_nf4_quant_b300._lib import lsn_step_opts
+    for bad in (-1, 3):
+        o = lsn_step_opts(0, 0)
+        o.bwd_weights = bad
+        assert _step_ex(o) == lsn.LSN_EINVAL
+        assert "bwd_weights" in _msg()
+    d = lsn.StackDesc(n_layers=2, d_model=256, d_kv=256, d_ff=512, rank=8)
+    nf4, dense = d.workspace_bytes(64, bwd_weights=1), d.workspace_bytes(64, bwd_weights=2)
+    # the bf16 scratch holds the larger of [W_o, W_down] and [W_q .. W_up]
+    assert dense - nf4 >= 2 * 256 * (256 + 256 + 256 + 512 + 512)
+    assert d.workspace_bytes(64) == nf4                    # automatic: NF4 operands below 8192 tokens
+    assert d.workspace_bytes(8192) == d.workspace_bytes(8192, bwd_weights=2)
+
+
 def test_sum_ranks_arguments_are_validated():
     P = C.c_void_p
     s = lsn.lib.lsn_sum_ranks

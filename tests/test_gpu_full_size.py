@@ -37,6 +37,16 @@ def full():
     return st, st.run()
 
 
+def test_decoded_weight_backward_matches_nf4_operands(full):
+    """At 16384 tokens the backward decodes each layer's W to bf16 by default; the run with
+    NF4 operands decoded inside the GEMMs gives the same bits."""
+    st, out = full
+    nf4 = st.run(bwd_weights=1)
+    assert torch.equal(out["dx0"].view(torch.int32), nf4["dx0"].view(torch.int32))
+    assert torch.equal(out["grads"][0].view(torch.int32), nf4["grads"][0].view(torch.int32))
+    assert torch.equal(out["loss"].view(torch.int32), nf4["loss"].view(torch.int32))
+
+
 def test_sampled_rows_match_oracle(full):
     from oracle.nf4 import bf16_value
     st, out = full

@@ -45,7 +45,7 @@ class Stack:
             pool.set_chunks(self.desc.chunk_offsets())
         return pool
 
-    def run(self, pool=None, recompute=False, reference=False):
+    def run(self, pool=None, recompute=False, reference=False, bwd_weights=0):
         lsn = _lsn()
         d = self.desc
         grads = [torch.full((d.lora_elems,), float("nan"), dtype=torch.float32, device="cuda")
@@ -55,11 +55,13 @@ class Stack:
         dx0 = torch.empty((self.M, d.d_model), dtype=torch.float32, device="cuda")
         x_ref = torch.empty((self.M, d.d_model), dtype=torch.bfloat16, device="cuda") if reference else None
         ws = self.ws
-        if recompute or reference:
-            ws = torch.empty(d.workspace_bytes(self.M, recompute, reference), dtype=torch.uint8, device="cuda")
+        if recompute or reference or bwd_weights:
+            ws = torch.empty(d.workspace_bytes(self.M, recompute, reference, bwd_weights), dtype=torch.uint8,
+                             device="cuda")
         lsn.layer_stack_step(d, self.x0, self.lora, grads, loss, ws, pool=pool,
                              resident_store=None if pool else self.resident, x_out=x_out, dx0=dx0,
-                             recompute=recompute, reference_pass=reference, x_ref_out=x_ref)
+                             recompute=recompute, reference_pass=reference, x_ref_out=x_ref,
+                             bwd_weights=bwd_weights)
         torch.cuda.synchronize()
         assert lsn.device_check() == 0
         return {"loss": loss, "x": x_out, "dx0": dx0, "grads": grads, "x_ref": x_ref}
@@ -146,6 +148,18 @@ def test_small_replay_slot_parity_and_delays(small):
     _same(base, small.run(pool))
     assert pool.stats()["skipped"] == 2
     pool.close()
+
+
+def test_decoded_weight_backward_bit_identical(small):
+    """bwd_weights = 2 decodes each layer's W to bf16 scratch and runs the backward's
+    transposed GEMMs on the dense copy; the decode gives the producers' values bit for bit, so
+    the step's results equal the NF4-operand run's, resident and streamed."""
+    base = small.run(bwd_weights=1)
+    _same(base, small.run(bwd_weights=2))
+    pool = small.pool()
+    _same(base, small.run(pool, bwd_weights=2))
+    pool.close()
+    _same(base, small.run(recompute=True, bwd_weights=2))
 
 
 def test_recompute_bit_identical_to_stored_activations(small):
