@@ -379,15 +379,16 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     compute = torch.cuda.Stream(device=dev)
     dp = lsn.DataParallel(pg, desc, grads, compute) if world > 1 else None
 
-    def step():
+    def step(x=None):
+        x = x0 if x is None else x
         kw = dict(stream=compute, recompute=recompute, reference_pass=ref_pass, x_ref_out=x_ref,
                   bwd_weights=bwd_weights)
         if dp is not None:
             kw.update(token_count=world * M, grads_ready=dp.hook)
         if resident is not None:
-            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, resident_store=resident, **kw)
+            lsn.layer_stack_step(desc, x, lora, grads, loss, ws, resident_store=resident, **kw)
         else:
-            lsn.layer_stack_step(desc, x0, lora, grads, loss, ws, pool=pool, **kw)
+            lsn.layer_stack_step(desc, x, lora, grads, loss, ws, pool=pool, **kw)
         if dp is not None:
             dp.finish()
 
@@ -428,12 +429,30 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     lsn.device_check(compute)
 
     # ------------------------------------------------------------------ end to end
+    # Every step's input comes from pinned host memory and its loss goes back to pinned host
+    # memory.  The next step's input is copied on a side stream into the other of two device
+    # buffers while the current step runs; a copy into a buffer waits for the step that last
+    # read it, and a step waits for its input's copy.
+    x0b = [x0, torch.empty_like(x0)]
+    copy_in = torch.cuda.Stream(device=dev)
+    landed = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        with torch.cuda.stream(compute):
-            x0.copy_(x0_host, non_blocking=True)
-        step()
+    with torch.cuda.stream(copy_in):
+        x0b[0].copy_(x0_host, non_blocking=True)
+    landed[0].record(copy_in)
+    for i in range(e2e_steps):
+        cur, nxt = i % 2, (i + 1) % 2
+        if i + 1 < e2e_steps:
+            if i >= 1:
+                copy_in.wait_event(used[nxt])   # step i - 1 read x0b[nxt]
+            with torch.cuda.stream(copy_in):
+                x0b[nxt].copy_(x0_host, non_blocking=True)
+            landed[nxt].record(copy_in)
+        compute.wait_event(landed[cur])
+        step(x0b[cur])
+        used[cur].record(compute)
         with torch.cuda.stream(compute):
             loss_host.copy_(loss, non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -441,7 +460,7 @@ def measure(torch, lsn, dev, desc, M, steps, warmup, pool, resident, lora, ref_p
     out = {"ms": ms, "launches": launches, "pstats": pstats, "prof": prof, "gemm_steps": gemm_steps,
            "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "clocks": clk.summary(), "x0_bytes": x0.numel() * 2,
            "loss": float(loss_host.item())}
-    del ws, grads, x_ref, dp
+    del ws, grads, x_ref, dp, x0b
     torch.cuda.empty_cache()
     return out
 
