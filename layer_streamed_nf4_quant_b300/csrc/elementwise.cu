@@ -341,30 +341,20 @@ __global__ void loss_final_kernel(const float* __restrict__ xpart, const float* 
 
 // ------------------------------------------------------------- backward dY assembly
 
-// dY_cat = [dq | dk | dv | dgate | dup] (bf16) from dqa = [dq | da] (fp32), the forward
-// outputs (k, v, gate, up) and the k/v loss coefficient.
-__global__ void dy_build_kernel(const float* __restrict__ dqa, const uint16_t* __restrict__ y,
+// dY_cat's [dk | dv | dgate | dup] columns (bf16) from da (fp32 [M x F]), the forward outputs
+// (k, v, gate, up) and the k/v loss coefficient; the dq columns come from the GEMM.
+__global__ void dy_build_kernel(const float* __restrict__ da_in, const uint16_t* __restrict__ y,
                                 uint16_t* __restrict__ dy, int M, int D, int dkv, int F, float kv_coef) {
-    const int ldq = D + F;
     const int ldy = D + 2 * dkv + 2 * F;
     const int ok = D, og = D + 2 * dkv, ou = og + F;   // v follows k directly
-    const int per_row = D / 8 + (2 * dkv) / 8 + F / 8;
+    const int per_row = (2 * dkv) / 8 + F / 8;
     const int64_t total = (int64_t)M * per_row;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = i / per_row;
         int c = (int)(i - row * per_row) * 8;
-        const float* dr = dqa + row * ldq;
         const uint16_t* yr = y + row * ldy;
         uint16_t* orow = dy + row * ldy;
-        if (c < D) {
-            const float4 a0 = *reinterpret_cast<const float4*>(dr + c);
-            const float4 a1 = *reinterpret_cast<const float4*>(dr + c + 4);
-            *reinterpret_cast<uint4*>(orow + c) =
-                make_uint4(bf2(a0.x, a0.y), bf2(a0.z, a0.w), bf2(a1.x, a1.y), bf2(a1.z, a1.w));
-            continue;
-        }
-        c -= D;
         if (c < 2 * dkv) {
             const int col = ok + c;   // k block then v block are adjacent
             const uint4 v = *reinterpret_cast<const uint4*>(yr + col);
@@ -376,8 +366,9 @@ __global__ void dy_build_kernel(const float* __restrict__ dqa, const uint16_t* _
             continue;
         }
         c -= 2 * dkv;
-        const float4 a0 = *reinterpret_cast<const float4*>(dr + D + c);
-        const float4 a1 = *reinterpret_cast<const float4*>(dr + D + c + 4);
+        const float* dr = da_in + row * F;
+        const float4 a0 = *reinterpret_cast<const float4*>(dr + c);
+        const float4 a1 = *reinterpret_cast<const float4*>(dr + c + 4);
         const float da[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const uint4 g4 = *reinterpret_cast<const uint4*>(yr + og + c);
         const uint4 u4 = *reinterpret_cast<const uint4*>(yr + ou + c);
@@ -497,10 +488,10 @@ int launch_loss(const uint16_t* x, int M, double norm_tokens, int D, int dkv, in
     return LSN_OK;
 }
 
-int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
+int launch_dy_build(const float* da, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
                     float kv_coef, cudaStream_t s) {
-    const int64_t work = (int64_t)M * (D / 8 + 2 * dkv / 8 + F / 8);
-    dy_build_kernel<<<grid_for(work, 256), 256, 0, s>>>(dqa, y, dy, M, D, dkv, F, kv_coef);
+    const int64_t work = (int64_t)M * (2 * dkv / 8 + F / 8);
+    dy_build_kernel<<<grid_for(work, 256), 256, 0, s>>>(da, y, dy, M, D, dkv, F, kv_coef);
     note_launch();
     LSN_CUDA_TRY(cudaGetLastError());
     return LSN_OK;

@@ -48,7 +48,7 @@ struct Buffers {
     float* dx = nullptr;
     uint16_t* dx_bf = nullptr;
     uint16_t* dtod = nullptr;
-    float* dqa = nullptr;
+    float* da = nullptr;   // dloss/da (fp32 [M x F]); dq goes straight into dY_cat as bf16
     uint16_t* dy = nullptr;
     uint16_t* dtcat = nullptr;
     float* dh = nullptr;
@@ -153,7 +153,7 @@ size_t layout(const Dims& d, uint8_t* base, const uint16_t* x0, Buffers* b, size
     b->dx = reinterpret_cast<float*>(take(M * d.D * 4));
     b->dx_bf = reinterpret_cast<uint16_t*>(take(M * d.D * 2));
     b->dtod = reinterpret_cast<uint16_t*>(take(M * 2 * d.r * 2));
-    b->dqa = reinterpret_cast<float*>(take(M * (d.D + d.F) * 4));
+    b->da = reinterpret_cast<float*>(take(M * d.F * 4));
     b->dy = reinterpret_cast<uint16_t*>(take(M * d.Ncat * 2));
     b->dtcat = reinterpret_cast<uint16_t*>(take(M * 5 * d.r * 2));
     b->dh = reinterpret_cast<float*>(take(M * d.D * 4));
@@ -381,16 +381,17 @@ int bwd_layer(Ctx& c, int l, const uint8_t* img, const uint16_t* lora, float* gr
         g.seg(mq_mn, 0, B_TMA_MN, mdtod_mn, 0, 0, M);
         g.problem(F, r, 64, A_MNMAJOR, EPI_F32_T, c.dA(grad, kDown), F, 1.0f, r, ws);
         g.seg(ma_mn, 0, B_TMA_MN, mdtod_mn, 0, r, M);
-        g.problem(M, D, 256, A_KMAJOR, EPI_F32, b.dqa, D + F, 1.0f, D, xs);
+        // dq: only its bf16 rounding is used (as dY_q), so it is written into dY_cat directly
+        g.problem(M, D, 256, A_KMAJOR, EPI_BF16, b.dy, d.Ncat, 1.0f, D, xs);
         g.seg(mdx, 0, bsrc, vo, 0, 0, D);
         g.seg(mdtod, 0, B_TMA_MN, mao, 0, 0, r, true);
-        g.problem(M, F, 256, A_KMAJOR, EPI_F32, b.dqa ? b.dqa + D : nullptr, D + F, 1.0f, F, xs);
+        g.problem(M, F, 256, A_KMAJOR, EPI_F32, b.da, F, 1.0f, F, xs);
         g.seg(mdx, 0, bsrc, vd, 0, 0, D);
         g.seg(mdtod, r, B_TMA_MN, mad, 0, 0, r, true);
         RC(c.run(g));
     }
     if (!c.dry)
-        RC(launch_dy_build(b.dqa, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / (d.norm_M * d.dkv)), c.s));
+        RC(launch_dy_build(b.da, b.y[l], b.dy, M, D, d.dkv, F, (float)(2.0 * d.coef / (d.norm_M * d.dkv)), c.s));
     RC(c.need_qkvgu());
     if (!c.dry) RC(launch_tag_check(img, (uint32_t)l, c.s));
     if (dense) RC(c.decode(img, kQ, kUp));

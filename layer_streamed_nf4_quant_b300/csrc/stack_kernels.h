@@ -29,8 +29,9 @@ int launch_loss(const uint16_t* x, int M, double norm_tokens, int D, int dkv, in
                 uint16_t* dx_bf, float* xpart, const float* kvpart, float* loss, cudaStream_t s);
 // out = in[0] + in[1] + ... (rank order, fp32), in = [n_ranks][n].
 int launch_sum_ranks(const float* in, int n_ranks, int64_t n, float* out, cudaStream_t s);
-// dY_cat = [dq | 2c k/(M dkv) | 2c v/(M dkv) | dgate | dup] in bf16.
-int launch_dy_build(const float* dqa, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
+// The k, v, gate and up columns of dY_cat (bf16): 2c k/(M dkv), 2c v/(M dkv), dgate, dup,
+// from da (fp32 [M x F]) and the forward outputs; the dq columns are written by the GEMM.
+int launch_dy_build(const float* da, const uint16_t* y, uint16_t* dy, int M, int D, int dkv, int F,
                     float kv_coef, cudaStream_t s);
 
 // One AdamW step over n fp32 parameters (bf16 copy into pb when non-null).
