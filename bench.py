@@ -522,7 +522,7 @@ def main(argv=None):
                     help="copies per layer image: 2 = [header, q..up] and [o, down] (sub-layer streaming), "
                          "1 = whole-layer copies")
     ap.add_argument("--bwd-weights", type=int, default=0, choices=[0, 1, 2],
-                    help="backward GEMMs' W: 0 automatic, 1 NF4 decoded in the GEMM, 2 decoded to bf16 first")
+                    help="backward GEMMs' W: 0/1 NF4 decoded in the GEMM (default), 2 decoded to bf16 first")
     ap.add_argument("--show-ranks", action="store_true",
                     help="print each rank's world size, rank and device binding as JSON and exit")
     args = ap.parse_args(argv)

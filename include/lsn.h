@@ -356,10 +356,10 @@ typedef struct {
     int32_t recompute;
     int32_t reference_pass;
     /* How the backward's two transposed GEMMs ([dq | da] and dh) read W:
-     *   1: packed NF4, decoded by the GEMM's producer warps into its operand tiles;
+     *   0 or 1: packed NF4, decoded by the GEMM's producer warps into its operand tiles (bf16
+     *      W never exists in HBM);
      *   2: each layer's W decoded once into bf16 scratch in the workspace (the same values,
-     *      bit for bit, so the results are identical), then read by TMA as a dense operand;
-     *   0: 2 from 8192 tokens up, else 1.
+     *      bit for bit, so the results are identical), then read by TMA as a dense operand.
      * Other values: LSN_EINVAL.  The workspace size depends on it (lsn_stack_workspace_bytes_ex). */
     int32_t bwd_weights;
     int32_t reserved[5];

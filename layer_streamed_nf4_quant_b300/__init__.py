@@ -407,8 +407,8 @@ def layer_stack_step(desc: StackDesc, x0, lora_blobs, grad_blobs, loss_out, ws, 
     token_count: the token count the loss means are taken over (0: M; a data-parallel shard
     passes the global batch's).
     grads_ready: a lsn_layer_hook (e.g. DataParallel's) called after each layer's backward.
-    bwd_weights: 0 automatic, 1 NF4 decoded inside the backward GEMMs, 2 each layer's weights
-    decoded to bf16 scratch first (identical results; size ws with the same value)."""
+    bwd_weights: 0 or 1 NF4 decoded inside the backward GEMMs, 2 each layer's weights decoded to
+    bf16 scratch first (identical results; size ws with the same value)."""
     L = desc.n_layers
     lo = (C.c_void_p * L)(*[b.data_ptr() for b in lora_blobs])
     gr = (C.c_void_p * L)(*[g.data_ptr() for g in grad_blobs])

@@ -96,14 +96,9 @@ bool make_dims(const lsn_stack_desc* d, int64_t M, Dims* o) {
     return true;
 }
 
-// Tokens from which the backward decodes each layer's weights to bf16 once and runs its two
-// transposed GEMMs on them (bwd_weights = 0): the decode costs about 0.1 ms per layer, and the
-// dense operand makes those GEMMs about 10 % faster, which pays from a few thousand tokens.
-constexpr int kDenseBwdTokens = 8192;
-
-bool dense_bwd(const Dims& d, const lsn_step_opts& o) {
-    return o.bwd_weights == 2 || (o.bwd_weights == 0 && d.M >= kDenseBwdTokens);
-}
+// The backward reads packed NF4 inside its GEMMs unless the caller asks for each layer's W to
+// be decoded to bf16 scratch first (bwd_weights = 2).
+bool dense_bwd(const Dims&, const lsn_step_opts& o) { return o.bwd_weights == 2; }
 
 // bf16 elements of the decoded-weight scratch: the larger of [W_o, W_down] and [W_q .. W_up].
 size_t wdec_elems(const Dims& d) {

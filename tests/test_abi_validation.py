@@ -160,8 +160,8 @@ def test_backward_weight_mode_is_validated_and_sized():
     nf4, dense = d.workspace_bytes(64, bwd_weights=1), d.workspace_bytes(64, bwd_weights=2)
     # the bf16 scratch holds the larger of [W_o, W_down] and [W_q .. W_up]
     assert dense - nf4 >= 2 * 256 * (256 + 256 + 256 + 512 + 512)
-    assert d.workspace_bytes(64) == nf4                    # automatic: NF4 operands below 8192 tokens
-    assert d.workspace_bytes(8192) == d.workspace_bytes(8192, bwd_weights=2)
+    assert d.workspace_bytes(64) == nf4                    # default: NF4 operands, no bf16 W
+    assert d.workspace_bytes(8192) == d.workspace_bytes(8192, bwd_weights=1)
 
 
 def test_sum_ranks_arguments_are_validated():

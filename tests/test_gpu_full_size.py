@@ -38,10 +38,10 @@ def full():
 
 
 def test_decoded_weight_backward_matches_nf4_operands(full):
-    """At 16384 tokens the backward decodes each layer's W to bf16 by default; the run with
-    NF4 operands decoded inside the GEMMs gives the same bits."""
+    """At 16384 tokens, the backward with each layer's W decoded to bf16 first (bwd_weights = 2)
+    gives the bits of the default run, whose GEMMs decode NF4 themselves."""
     st, out = full
-    nf4 = st.run(bwd_weights=1)
+    nf4 = st.run(bwd_weights=2)
     assert torch.equal(out["dx0"].view(torch.int32), nf4["dx0"].view(torch.int32))
     assert torch.equal(out["grads"][0].view(torch.int32), nf4["grads"][0].view(torch.int32))
     assert torch.equal(out["loss"].view(torch.int32), nf4["loss"].view(torch.int32))
